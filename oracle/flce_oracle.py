@@ -1,0 +1,212 @@
+"""Plain, slow, fp64 statement of what the fused LM-head cross-entropy computes.
+
+TEST INFRASTRUCTURE: only tests, the smoke check and the benchmark's CPU
+baseline may use this module. It shares no code with the CUDA library.
+
+Notation (Trillion Labs note, "Cross Entropy를 다시 보면"; PyTorch 2.13
+LinearCrossEntropyLoss chapter, "먼저 수식에서 없앨 수 있는 tensor를 찾는다"):
+H [N,D] hidden rows, W [V,D] LM-head weight, y [N] targets with
+ignore_index = -100.
+
+    z_n     = H_n W^T                              (one logit row)
+    LSE_n   = m_n + log sum_v exp(z_nv - m_n),      m_n = max_v z_nv
+    loss    = sum_{valid n} (LSE_n - z_{n,y_n}) / count    (0 when count = 0)
+    dZ_nv   = (g / count) * valid_n * (exp(z_nv - LSE_n) - [v = y_n])
+    dH      = dZ W,   dW = dZ^T H
+
+The stable max-shifted LSE is the one Cut Cross-Entropy prescribes
+("Cut Your Losses in Large-Vocabulary Language Models", Sec. 4.2, Alg. 2);
+the softmax in the backward is exp(z - LSE) with no renormalisation (Sec. 4.3).
+The loss is the negative of that paper's Eq. 4 log-likelihood, averaged over
+non-ignored rows with the count clamped to at least one (the note's chunked
+cross-entropy listing divides by count.clamp_min(1)), so dZ is
+softmax - onehot (the note's and the chapter's gradient formula) rather than
+the paper's onehot - softmax (Alg. 4).
+
+All arithmetic is fp64 on exactly widened bf16 inputs; matrix products use the
+library matmul. Rows are processed in blocks only to bound memory: every
+output element is still one plain sum.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+IGNORE_INDEX = -100
+_BLOCK_BYTES = 256 << 20
+
+
+def inputs_f64(h_bits: np.ndarray, w_bits: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Widen bf16 bit patterns (uint16) to fp64 exactly."""
+    def widen(b):
+        return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(
+            np.float32).astype(np.float64)
+    return widen(h_bits), widen(w_bits)
+
+
+def _row_blocks(n: int, vocab: int):
+    step = max(1, _BLOCK_BYTES // max(1, vocab * 8))
+    for r0 in range(0, n, step):
+        yield r0, min(n, r0 + step)
+
+
+def logits(H: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """z = H W^T in fp64 (the LM-head projection)."""
+    return np.asarray(H, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T
+
+
+def logsumexp_rows(z: np.ndarray) -> np.ndarray:
+    """Per-row log-sum-exp, shifted by the row maximum for stability."""
+    m = z.max(axis=1)
+    return m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+
+
+def valid_count(y: np.ndarray, ignore_index: int = IGNORE_INDEX) -> int:
+    return int(np.count_nonzero(np.asarray(y) != ignore_index))
+
+
+def _check_targets(y, vocab, ignore_index):
+    y = np.asarray(y, dtype=np.int64)
+    bad = (y != ignore_index) & ((y < 0) | (y >= vocab))
+    if np.any(bad):
+        raise ValueError("target outside [0, V) that is not ignore_index")
+    return y
+
+
+def lse_rows(H: np.ndarray, W: np.ndarray, rows) -> np.ndarray:
+    """LSE_n for the listed rows only (each needs just H_n and all of W)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.empty(rows.shape[0], dtype=np.float64)
+    for r0, r1 in _row_blocks(rows.shape[0], W.shape[0]):
+        out[r0:r1] = logsumexp_rows(logits(H[rows[r0:r1]], W))
+    return out
+
+
+def forward(H: np.ndarray, W: np.ndarray, y: np.ndarray, ignore_index: int = IGNORE_INDEX):
+    """Per-row LSE, mean loss over valid rows and the valid count."""
+    n, vocab = H.shape[0], W.shape[0]
+    y = _check_targets(y, vocab, ignore_index)
+    lse = np.empty(n, dtype=np.float64)
+    total = 0.0
+    for r0, r1 in _row_blocks(n, vocab):
+        z = logits(H[r0:r1], W)
+        lse[r0:r1] = logsumexp_rows(z)
+        for i in range(r1 - r0):
+            t = y[r0 + i]
+            if t != ignore_index:
+                total += lse[r0 + i] - z[i, t]
+    count = valid_count(y, ignore_index)
+    loss = total / max(count, 1)
+    return lse, loss, count
+
+
+def loss_value(H, W, y, ignore_index: int = IGNORE_INDEX) -> float:
+    return forward(H, W, y, ignore_index)[1]
+
+
+def _dlogits_block(z, lse_blk, y_blk, scale, ignore_index):
+    dz = np.exp(z - lse_blk[:, None])
+    for i in range(z.shape[0]):
+        t = y_blk[i]
+        if t == ignore_index:
+            dz[i, :] = 0.0
+        else:
+            dz[i, t] -= 1.0
+    return dz * scale
+
+
+def dlogits(H, W, y, grad_loss: float = 1.0, ignore_index: int = IGNORE_INDEX) -> np.ndarray:
+    """The full dZ [N,V] (small inputs only: this is the array the method avoids)."""
+    y = _check_targets(y, W.shape[0], ignore_index)
+    z = logits(H, W)
+    lse = logsumexp_rows(z)
+    scale = grad_loss / max(valid_count(y, ignore_index), 1)
+    return _dlogits_block(z, lse, y, scale, ignore_index)
+
+
+def forward_backward(H, W, y, grad_loss: float = 1.0, ignore_index: int = IGNORE_INDEX):
+    """LSE [N], loss, dH [N,D], dW [V,D], count; no [N,V] array beyond a row block."""
+    n, vocab = H.shape[0], W.shape[0]
+    y = _check_targets(y, vocab, ignore_index)
+    count = valid_count(y, ignore_index)
+    scale = grad_loss / max(count, 1)
+    lse = np.empty(n, dtype=np.float64)
+    dH = np.zeros(H.shape, dtype=np.float64)
+    dW = np.zeros(W.shape, dtype=np.float64)
+    total = 0.0
+    for r0, r1 in _row_blocks(n, vocab):
+        z = logits(H[r0:r1], W)
+        lse[r0:r1] = logsumexp_rows(z)
+        for i in range(r1 - r0):
+            t = y[r0 + i]
+            if t != ignore_index:
+                total += lse[r0 + i] - z[i, t]
+        dz = _dlogits_block(z, lse[r0:r1], y[r0:r1], scale, ignore_index)
+        dH[r0:r1] = dz @ W
+        dW += dz.T @ H[r0:r1]
+    loss = total / max(count, 1)
+    return lse, loss, dH, dW, count
+
+
+def dH_rows(H, W, y, rows, grad_loss: float = 1.0, ignore_index: int = IGNORE_INDEX):
+    """dH_n for the listed rows: needs LSE_n, the global valid count and W."""
+    y = _check_targets(y, W.shape[0], ignore_index)
+    rows = np.asarray(rows, dtype=np.int64)
+    scale = grad_loss / max(valid_count(y, ignore_index), 1)
+    out = np.empty((rows.shape[0], W.shape[1]), dtype=np.float64)
+    for r0, r1 in _row_blocks(rows.shape[0], W.shape[0]):
+        sel = rows[r0:r1]
+        z = logits(H[sel], W)
+        dz = _dlogits_block(z, logsumexp_rows(z), y[sel], scale, ignore_index)
+        out[r0:r1] = dz @ W
+    return out
+
+
+def dW_rows(H, W, y, lse, vocab_ids, grad_loss: float = 1.0, ignore_index: int = IGNORE_INDEX):
+    """dW_v for the listed vocabulary rows, given the oracle's own LSE of all rows.
+
+    dW_v = (g / count) sum_{valid n} (exp(z_nv - LSE_n) - [y_n = v]) H_n.
+    """
+    y = _check_targets(y, W.shape[0], ignore_index)
+    vocab_ids = np.asarray(vocab_ids, dtype=np.int64)
+    scale = grad_loss / max(valid_count(y, ignore_index), 1)
+    zc = logits(H, W[vocab_ids])                       # [N, k]
+    p = np.exp(zc - np.asarray(lse, dtype=np.float64)[:, None])
+    valid = y != ignore_index
+    p[~valid, :] = 0.0
+    for j, v in enumerate(vocab_ids):
+        p[valid & (y == v), j] -= 1.0
+    return scale * (p.T @ H)
+
+
+def forward_backward_filtered(H, W, y, eps: float, tile_rows: int, tile_cols: int,
+                              grad_loss: float = 1.0, ignore_index: int = IGNORE_INDEX):
+    """Gradient filtering of Cut Cross-Entropy Alg. 4, emulated in fp64.
+
+    The dZ matrix is cut into tile_rows x tile_cols tiles aligned at 0; a tile
+    whose unscaled gradient G = softmax - onehot has every |G| < eps (ignored
+    rows count as G = 0) contributes nothing to dH or dW. Returns the same
+    tuple as forward_backward plus the fraction of tiles skipped.
+    """
+    n, vocab = H.shape[0], W.shape[0]
+    y = _check_targets(y, vocab, ignore_index)
+    count = valid_count(y, ignore_index)
+    scale = grad_loss / max(count, 1)
+    lse, loss, _ = forward(H, W, y, ignore_index)
+    dH = np.zeros(H.shape, dtype=np.float64)
+    dW = np.zeros(W.shape, dtype=np.float64)
+    tiles = skipped = 0
+    for r0 in range(0, n, tile_rows):
+        r1 = min(n, r0 + tile_rows)
+        z = logits(H[r0:r1], W)
+        g = _dlogits_block(z, lse[r0:r1], y[r0:r1], 1.0, ignore_index)
+        for c0 in range(0, vocab, tile_cols):
+            c1 = min(vocab, c0 + tile_cols)
+            tiles += 1
+            if np.all(np.abs(g[:, c0:c1]) < eps):
+                skipped += 1
+                g[:, c0:c1] = 0.0
+        dz = g * scale
+        dH[r0:r1] = dz @ W
+        dW += dz.T @ H[r0:r1]
+    return lse, loss, dH, dW, count, skipped / max(tiles, 1)

@@ -1,0 +1,225 @@
+"""Pins for the fp64 oracle: closed forms, invariants, a library cross-check,
+finite differences and symmetries. None of these re-uses the oracle's code.
+
+The facts pinned come from the pages: the loss is logsumexp(z) - z_y with
+z = h W^T and gradient softmax - onehot (Trillion Labs note, "Cross Entropy를
+다시 보면"); the mean is over non-ignored rows with the count clamped to one
+(the note's chunked cross-entropy listing); dH = dZ W and dW = dZ^T H
+(PyTorch 2.13 LinearCrossEntropyLoss chapter, "먼저 수식에서 없앨 수 있는 tensor를
+찾는다"); softmax = exp(z - LSE) (Cut Cross-Entropy, Sec. 4.3).
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+IGN = -100
+
+
+def _rand(seed, n, d, v, w_scale=0.5, ignore=()):
+    rng = np.random.default_rng(seed)
+    H = rng.standard_normal((n, d))
+    W = rng.standard_normal((v, d)) * w_scale
+    y = rng.integers(0, v, size=n).astype(np.int64)
+    for i in ignore:
+        y[i] = IGN
+    return H, W, y
+
+
+def test_w_zero_gives_log_v_and_closed_form_gradients():
+    n, d, v = 7, 5, 13
+    H, _, y = _rand(1, n, d, v, ignore=(2, 5))
+    W = np.zeros((v, d))
+    g = 1.7
+    lse, loss, dH, dW, count = oracle.forward_backward(H, W, y, grad_loss=g)
+    assert count == 5
+    assert np.all(np.abs(lse - math.log(v)) < 1e-14)
+    assert abs(loss - math.log(v)) < 1e-14
+    assert np.all(dH == 0.0)
+    # dW_v = (g/count) * sum_{valid n} (1/V - [y_n = v]) H_n, written out by loops.
+    expect = np.zeros((v, d))
+    for vv in range(v):
+        for i in range(n):
+            if y[i] == IGN:
+                continue
+            coef = 1.0 / v - (1.0 if y[i] == vv else 0.0)
+            for k in range(d):
+                expect[vv, k] += coef * H[i, k]
+    expect *= g / count
+    assert np.max(np.abs(dW - expect)) < 1e-13
+
+
+def test_w_zero_headline_vocab_value():
+    # log(151552) for the Gravity-16B-A3B vocabulary.
+    H = np.ones((2, 8))
+    W = np.zeros((151552, 8))
+    lse, loss, _ = oracle.forward(H, W, np.array([3, 151551]))
+    assert abs(loss - 11.9286841) < 1e-6
+    assert abs(lse[0] - math.log(151552)) < 1e-13
+
+
+def test_dz_rows_sum_to_zero_and_ignored_rows_are_zero():
+    H, W, y = _rand(2, 9, 6, 31, w_scale=1.0, ignore=(0, 4))
+    g = 3.0
+    dz = oracle.dlogits(H, W, y, grad_loss=g)
+    count = 7
+    for i in range(9):
+        if y[i] == IGN:
+            assert np.all(dz[i] == 0.0)
+        else:
+            assert abs(dz[i].sum()) < 1e-14
+            assert dz[i, y[i]] < 0
+            assert np.all(dz[i] >= -g / count - 1e-15)
+            assert np.all(dz[i] <= g / count + 1e-15)
+
+
+def test_ignored_rows_have_exactly_zero_dh():
+    H, W, y = _rand(3, 12, 8, 40, ignore=(1, 7, 11))
+    _, _, dH, _, _ = oracle.forward_backward(H, W, y)
+    for i in (1, 7, 11):
+        assert np.all(dH[i] == 0.0)
+    assert np.all(np.abs(dH[0]) > 0)
+
+
+def test_central_finite_differences():
+    n, d, v = 6, 5, 11
+    H, W, y = _rand(4, n, d, v, w_scale=1.0, ignore=(3,))
+    _, _, dH, dW, _ = oracle.forward_backward(H, W, y)
+    h = 1e-6
+    for i in range(n):
+        for k in range(d):
+            Hp, Hm = H.copy(), H.copy()
+            Hp[i, k] += h
+            Hm[i, k] -= h
+            fd = (oracle.loss_value(Hp, W, y) - oracle.loss_value(Hm, W, y)) / (2 * h)
+            assert abs(fd - dH[i, k]) <= 1e-6 * max(1.0, abs(dH[i, k])) + 1e-9
+    for vv in range(v):
+        for k in range(d):
+            Wp, Wm = W.copy(), W.copy()
+            Wp[vv, k] += h
+            Wm[vv, k] -= h
+            fd = (oracle.loss_value(H, Wp, y) - oracle.loss_value(H, Wm, y)) / (2 * h)
+            assert abs(fd - dW[vv, k]) <= 1e-6 * max(1.0, abs(dW[vv, k])) + 1e-9
+
+
+@pytest.mark.parametrize("seed,n,d,v", [(5, 17, 12, 50), (6, 33, 8, 257), (7, 4, 3, 2)])
+def test_matches_explicit_full_logits_library_cross_entropy(seed, n, d, v):
+    H, W, y = _rand(seed, n, d, v, w_scale=2.0, ignore=(0,) if n > 1 else ())
+    Ht = torch.tensor(H, dtype=torch.float64, requires_grad=True)
+    Wt = torch.tensor(W, dtype=torch.float64, requires_grad=True)
+    z = Ht @ Wt.T
+    ref = torch.nn.functional.cross_entropy(z, torch.tensor(y), ignore_index=IGN, reduction="mean")
+    ref.backward()
+    lse_ref = torch.logsumexp(z.detach(), dim=1).numpy()
+    lse, loss, dH, dW, _ = oracle.forward_backward(H, W, y)
+    assert abs(loss - ref.item()) <= 1e-12 * max(1.0, abs(ref.item()))
+    assert np.max(np.abs(lse - lse_ref)) <= 1e-12 * max(1.0, np.max(np.abs(lse_ref)))
+    assert np.max(np.abs(dH - Ht.grad.numpy())) <= 1e-13
+    assert np.max(np.abs(dW - Wt.grad.numpy())) <= 1e-13
+
+
+def test_large_logits_are_stable():
+    H, W, y = _rand(8, 5, 4, 9, w_scale=300.0)
+    z = torch.tensor(H) @ torch.tensor(W).T
+    lse, loss, _ = oracle.forward(H, W, y)
+    assert np.all(np.isfinite(lse))
+    assert np.max(np.abs(lse - torch.logsumexp(z, 1).numpy())) < 1e-9
+
+
+def test_single_class_vocab_gives_zero_loss_and_gradients():
+    H, W, _ = _rand(9, 6, 4, 1)
+    y = np.zeros(6, dtype=np.int64)
+    lse, loss, dH, dW, _ = oracle.forward_backward(H, W, y)
+    assert np.max(np.abs(lse - (H @ W.T)[:, 0])) < 1e-14
+    assert abs(loss) < 1e-14
+    assert np.max(np.abs(dH)) < 1e-14 and np.max(np.abs(dW)) < 1e-14
+
+
+def test_all_rows_ignored_gives_zero_loss_and_gradients():
+    H, W, _ = _rand(10, 5, 4, 7)
+    y = np.full(5, IGN, dtype=np.int64)
+    lse, loss, dH, dW, count = oracle.forward_backward(H, W, y)
+    assert count == 0 and loss == 0.0
+    assert np.all(dH == 0.0) and np.all(dW == 0.0)
+    assert np.max(np.abs(lse - torch.logsumexp(torch.tensor(H @ W.T), 1).numpy())) < 1e-13
+
+
+def test_vocab_permutation_equivariance():
+    H, W, y = _rand(11, 10, 6, 23, ignore=(2,))
+    perm = np.random.default_rng(0).permutation(23)          # new row j holds old row perm[j]
+    inv = np.argsort(perm)
+    y2 = np.where(y == IGN, IGN, inv[np.where(y == IGN, 0, y)])
+    lse, loss, dH, dW, _ = oracle.forward_backward(H, W, y)
+    lse2, loss2, dH2, dW2, _ = oracle.forward_backward(H, W[perm], y2)
+    assert abs(loss - loss2) < 1e-13
+    assert np.max(np.abs(lse - lse2)) < 1e-13
+    assert np.max(np.abs(dH - dH2)) < 1e-13
+    assert np.max(np.abs(dW[perm] - dW2)) < 1e-13
+
+
+def test_row_permutation_equivariance():
+    H, W, y = _rand(12, 10, 6, 23, ignore=(2, 9))
+    perm = np.random.default_rng(1).permutation(10)
+    lse, loss, dH, dW, _ = oracle.forward_backward(H, W, y)
+    lse2, loss2, dH2, dW2, _ = oracle.forward_backward(H[perm], W, y[perm])
+    assert abs(loss - loss2) < 1e-13
+    assert np.max(np.abs(lse[perm] - lse2)) < 1e-13
+    assert np.max(np.abs(dH[perm] - dH2)) < 1e-13
+    assert np.max(np.abs(dW - dW2)) < 1e-13
+
+
+def test_grad_loss_scales_gradients_only():
+    H, W, y = _rand(13, 8, 5, 19)
+    _, l1, dH1, dW1, _ = oracle.forward_backward(H, W, y, grad_loss=1.0)
+    _, l2, dH2, dW2, _ = oracle.forward_backward(H, W, y, grad_loss=-2.5)
+    assert l1 == l2
+    assert np.max(np.abs(dH2 + 2.5 * dH1)) < 1e-14
+    assert np.max(np.abs(dW2 + 2.5 * dW1)) < 1e-14
+
+
+def test_inner_product_identity():
+    # <W, dW> = <H, dH> = sum_{n,v} dZ_nv z_nv: holds at any size, used for the
+    # long-context parity check where dW cannot be sampled.
+    H, W, y = _rand(14, 12, 7, 29, ignore=(3,))
+    _, _, dH, dW, _ = oracle.forward_backward(H, W, y)
+    assert abs(np.sum(W * dW) - np.sum(H * dH)) < 1e-13
+    # Column sums of dW vanish: softmax and onehot both sum to one per row.
+    assert np.max(np.abs(dW.sum(axis=0))) < 1e-13
+
+
+def test_out_of_range_target_rejected():
+    H, W, y = _rand(15, 3, 2, 5)
+    y[1] = 5
+    with pytest.raises(ValueError):
+        oracle.forward(H, W, y)
+
+
+def test_sampled_helpers_match_full_run():
+    H, W, y = _rand(16, 40, 9, 70, ignore=(1, 2, 30))
+    lse, _, dH, dW, _ = oracle.forward_backward(H, W, y, grad_loss=0.5)
+    rows = np.array([0, 2, 17, 39])
+    vocab_ids = np.array([0, 5, 69, int(y[0])])
+    assert np.max(np.abs(oracle.lse_rows(H, W, rows) - lse[rows])) < 1e-13
+    assert np.max(np.abs(oracle.dH_rows(H, W, y, rows, grad_loss=0.5) - dH[rows])) < 1e-14
+    assert np.max(np.abs(oracle.dW_rows(H, W, y, lse, vocab_ids, grad_loss=0.5) - dW[vocab_ids])) < 1e-14
+
+
+def test_filter_special_cases():
+    H, W, y = _rand(17, 20, 6, 64, w_scale=2.0, ignore=(4,))
+    full = oracle.forward_backward(H, W, y)
+    f0 = oracle.forward_backward_filtered(H, W, y, 0.0, 8, 16)
+    assert f0[5] == 0.0
+    assert np.array_equal(f0[2], full[2]) or np.max(np.abs(f0[2] - full[2])) < 1e-15
+    f_all = oracle.forward_backward_filtered(H, W, y, 2.0, 8, 16)
+    assert f_all[5] == 1.0
+    assert np.all(f_all[2] == 0.0) and np.all(f_all[3] == 0.0)
+    fracs = [oracle.forward_backward_filtered(H, W, y, e, 8, 16)[5] for e in (1e-6, 1e-3, 1e-1)]
+    assert fracs[0] <= fracs[1] <= fracs[2]
+    # A skipped tile drops exactly its own terms: rows outside skipped tiles of
+    # a one-row-tile filtering keep their exact dH.
+    f1 = oracle.forward_backward_filtered(H, W, y, 1e-3, 1, 64)
+    assert np.max(np.abs(f1[2] - full[2])) <= 1e-3 * np.max(np.abs(W)) * 64 / 19
