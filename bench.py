@@ -1,0 +1,376 @@
+#!/usr/bin/env python3
+"""Benchmark: fused LM-head projection + cross-entropy, forward and backward.
+
+One step = one flce_forward_backward call over one batch of synthetic rows
+(the Gravity-16B-A3B-shaped head by default: N = 8192, D = 2048,
+V = 151,552, bf16 inputs, fp32 outputs), with the inputs resident in HBM.
+W alone (592 MiB) is larger than the 129 MB L2, so no L2 flush is added
+between steps.
+
+Prints one JSON line (rank 0). Under torchrun every rank runs its own batch
+on its own GPU with no collective in the data path (weak scaling); the step
+time is the maximum over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores, on a bounded
+sample of the same workload, as the reference arm.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "fwd+bwd tokens/s & % BF16 tensor peak at V=151552 D=2048 N=8192"
+UNIT = "tokens/s"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gravity16b_head", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--filter-eps", type=float, default=0.0)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7], "sw_power": parts[8]})
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        loaded = [r for r in rows if r["power"] > 300.0] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(loaded),
+                "power_w_median": statistics.median(r["power"] for r in loaded)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(inp, target_seconds: float):
+    """Time the fp64 oracle (forward + backward) on the first S rows of the
+    batch with the full vocabulary; S grows until the run takes about
+    target_seconds. Returns tokens/s, the sample size and the core count."""
+    import oracle
+    H64, W64 = oracle.inputs_f64(inp["H"], inp["W"])
+    y = inp["y"]
+    rows = 16
+    while True:
+        t0 = time.perf_counter()
+        oracle.forward_backward(H64[:rows], W64, y[:rows])
+        dt = time.perf_counter() - t0
+        if dt >= target_seconds / 4 or rows >= H64.shape[0]:
+            break
+        rows = min(H64.shape[0], int(rows * max(2.0, min(8.0, target_seconds / 4 / max(dt, 1e-3)))))
+    return rows / dt, rows, dt
+
+
+def cpu_cores() -> int:
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ our path
+def run_ours(args, rank, world, local):
+    import torch
+    import torch.distributed as dist
+
+    import lm_head_loss_gb300 as flce
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(wl, seed=args.seed + rank)
+    N, D, V = wl.n_rows, wl.hidden, wl.vocab
+    H = torch.from_numpy(inp["H"].view(np.int16)).view(torch.bfloat16).to(dev)
+    W = torch.from_numpy(inp["W"].view(np.int16)).view(torch.bfloat16).to(dev)
+    y = torch.from_numpy(inp["y"]).to(dev)
+    prob = flce.make_problem(N, D, V, -100, args.filter_eps, 0)
+    ws_bytes = flce.flce_workspace_bytes(prob)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    loss = torch.empty((), dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    dH = torch.empty(N, D, dtype=torch.float32, device=dev)
+    dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        st = flce.flce_forward_backward(prob, H, W, y, 1.0, lse, loss, dH, dW, ws, stream=stream)
+        if st != flce.Status.OK:
+            raise flce.FlceError(st, "flce_forward_backward")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    torch.cuda.synchronize()
+    base_alloc = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    status = flce.flce_get_device_status(ws, stream)
+    if status != flce.Status.OK:
+        raise flce.FlceError(status, "device status after warm-up")
+    peak_extra = torch.cuda.max_memory_allocated(dev) - base_alloc
+
+    launches_per_step = 0
+    prof = flce.LaunchProfiler(capacity=4096)
+    with prof:
+        step()
+    torch.cuda.synchronize()
+    launches_per_step = prof.count
+
+    cap = launches_per_step * args.steps
+    prof = flce.LaunchProfiler(capacity=cap)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        with prof:
+            start.record(stream)
+            for _ in range(args.steps):
+                step()
+            end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    total_ms = start.elapsed_time(end)
+    per_kind = prof.summary()
+    clk = clocks.summary()
+
+    ms_t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    total_ms_max = float(ms_t.item())
+    ms_per_step = total_ms_max / args.steps
+    value = N * world * args.steps / (total_ms_max / 1e3)
+
+    flops_step = 8.0 * N * V * D
+    peaks, peak_src = measured_peaks()
+    gemm_ms = sum(v["ms"] for k, v in per_kind.items() if k.startswith("gemm_"))
+    gemm_launches = sum(v["launches"] for k, v in per_kind.items() if k.startswith("gemm_"))
+    achieved = flops_step * args.steps / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
+    peak = float(peaks["bf16_tflops_sustained"])
+    step_tflops = flops_step / (ms_per_step / 1e3) / 1e12
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "n_rows": N, "hidden": D, "vocab": V, "global_batch_rows": N * world,
+                   "targets": wl.targets, "ignore_frac": wl.ignore_frac, "filter_eps": args.filter_eps,
+                   "parallelism": f"dp{world} (independent batches, no collective)",
+                   "l2": "no flush: W (592 MiB bf16) alone exceeds the 129 MB L2 every step"},
+        "tflops": step_tflops,
+        "pct_bf16_peak": 100.0 * step_tflops / peak,
+        "pct_bf16_peak_burst": 100.0 * step_tflops / float(peaks["bf16_tflops"]),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": (achieved / peak) if achieved else None, "traffic": None,
+                     "kernel": "flce_gemm_kernel (all four epilogues)",
+                     "flops_per_launch": flops_step / (gemm_launches / args.steps) if gemm_launches else None,
+                     "launches_per_step": gemm_launches / args.steps if gemm_launches else None,
+                     "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)"},
+        "kernel_ms_per_step": {k: v["ms"] / args.steps for k, v in sorted(per_kind.items())},
+        "gpu_launches": prof.count,
+        "memory": {"workspace_mib": ws_bytes / 2 ** 20, "peak_extra_alloc_mib": peak_extra / 2 ** 20,
+                   "logits_avoided_mib": wl.logits_bytes_bf16() / 2 ** 20},
+        "clocks": clk,
+        "loss": float(loss.item()),
+    }
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, flce, torch, inp, prob, ws, (loss, lse, dH, dW), dev, stream, world, dist)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, rows, dt = oracle_sample(inp, args.cpu_seconds)
+        result["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                                  "sample": f"first {rows} rows of the batch, full V and D, fp64 forward+backward, "
+                                            f"{dt:.1f} s"}
+    return result
+
+
+def run_e2e(args, flce, torch, inp, prob, ws, outs, dev, stream, world, dist):
+    """Same step through the public API from pinned HOST buffers: every step
+    copies H, W and y to the device, runs the call, and reads the loss back."""
+    loss, lse, dH, dW = outs
+    hH = torch.from_numpy(inp["H"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    hW = torch.from_numpy(inp["W"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    hy = torch.from_numpy(inp["y"]).pin_memory()
+    hloss = torch.empty((), dtype=torch.float32).pin_memory()
+    H = torch.empty(hH.shape, dtype=torch.bfloat16, device=dev)
+    W = torch.empty(hW.shape, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(hy.shape, dtype=torch.int64, device=dev)
+
+    def step():
+        H.copy_(hH, non_blocking=True)
+        W.copy_(hW, non_blocking=True)
+        y.copy_(hy, non_blocking=True)
+        st = flce.flce_forward_backward(prob, H, W, y, 1.0, lse, loss, dH, dW, ws, stream=stream)
+        if st != flce.Status.OK:
+            raise flce.FlceError(st, "flce_forward_backward")
+        hloss.copy_(loss, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = torch.tensor([start.elapsed_time(end)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+    n = inp["H"].shape[0]
+    return {"value": n * world * args.steps / (float(ms.item()) / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": int(hH.numel() * 2 + hW.numel() * 2 + hy.numel() * 8),
+            "d2h_bytes_per_step": 4, "ms_per_step": float(ms.item()) / args.steps}
+
+
+# ------------------------------------------------------------------ reference arm
+def run_reference(args):
+    wl = synth.WORKLOADS[args.workload]
+    inp = synth.make_inputs(wl, seed=args.seed)
+    import oracle
+    H64, W64 = oracle.inputs_f64(inp["H"], inp["W"])
+    # Size one step to about (a few minutes) / (steps + warmup) of CPU time.
+    per_step_s = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    rows = 8
+    while True:
+        t0 = time.perf_counter()
+        oracle.forward_backward(H64[:rows], W64, inp["y"][:rows])
+        dt = time.perf_counter() - t0
+        if dt >= per_step_s / 2 or rows >= wl.n_rows:
+            break
+        rows = min(wl.n_rows, rows * 2)
+    for _ in range(args.warmup):
+        oracle.forward_backward(H64[:rows], W64, inp["y"][:rows])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.forward_backward(H64[:rows], W64, inp["y"][:rows])
+    total = time.perf_counter() - t0
+    value = rows * args.steps / total
+    sample = f"first {rows} rows of the batch per step, full V and D, fp64 forward+backward"
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "n_rows": wl.n_rows, "hidden": wl.hidden, "vocab": wl.vocab},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    result = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,147 @@
+/*
+ * flce.h -- fused LM-head projection + cross-entropy on one GB300 (sm_103a).
+ *
+ * The library computes, for hidden rows H [N,D], LM-head weight W [V,D] and
+ * targets y [N] (ignore_index marks rows that do not count):
+ *
+ *   z_n    = H_n W^T                                   (never stored)
+ *   LSE_n  = log sum_v exp(z_nv)
+ *   loss   = sum_{valid n} (LSE_n - z_{n,y_n}) / max(count, 1)
+ *   dZ     = grad_loss / max(count, 1) * valid * (softmax(z) - onehot(y))   (never stored whole)
+ *   dH     = dZ W,   dW = dZ^T H
+ *
+ * The loss and its gradient are the ones stated in the Trillion Labs note on
+ * Fused Linear Cross-Entropy ("Cross Entropy를 다시 보면": loss = -z(y) +
+ * log sum exp z, dL/dz = softmax(z) - 1[j = y]) and in the PyTorch 2.13
+ * LinearCrossEntropyLoss chapter ("먼저 수식에서 없앨 수 있는 tensor를 찾는다":
+ * dZ = softmax(Z) - one_hot(target), dH = dZ W, dW = dZ^T H). The mean runs
+ * over non-ignored rows with the count clamped to one (the note's chunked
+ * cross-entropy listing). The forward is the blockwise linear-log-sum-exp of
+ * "Cut Your Losses in Large-Vocabulary Language Models" (Sec. 4.2, Alg. 2)
+ * with the target logit gathered as in its indexed matmul (Sec. 4.1, Alg. 1);
+ * the backward recomputes logit tiles and forms softmax = exp(z - LSE) without
+ * renormalising (Sec. 4.3, Alg. 3 and 4). The full [N,V] logits and dlogits
+ * are never allocated.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers, row-major and contiguous, owned
+ *    by the caller. The library never allocates or frees device memory.
+ *  - H and W are bf16 (IEEE bfloat16 bit patterns, 2 bytes each), 16-byte
+ *    aligned, with D a multiple of 8 (row pitch of 16 bytes for TMA).
+ *  - Outputs lse, loss, dH, dW are fp32. dH and dW must be 16-byte aligned.
+ *  - ws is a caller-owned device workspace of at least
+ *    flce_workspace_bytes(p) bytes, 256-byte aligned. It holds the status
+ *    word, per-tile LSE partials, the per-row LSE when the caller passes no
+ *    lse buffer, and a bf16 staging buffer for a bounded chunk of dZ. Its size
+ *    grows with N + V, never with N * V.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call returns without synchronising. Errors found on the
+ *    host are returned before anything is launched. Errors found by the GPU
+ *    (a target outside [0,V) that is not ignore_index, a wait that ran out)
+ *    are recorded in the workspace's status word: such rows are treated as
+ *    ignored so all outputs stay finite, and flce_get_device_status reports
+ *    the error.
+ *  - Results are deterministic: the same inputs give bit-identical outputs.
+ */
+#ifndef FLCE_H_
+#define FLCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FLCE_OK = 0,
+  FLCE_ERR_INVALID_ARGUMENT = 1,   /* null pointer, negative size, bad flag or threshold */
+  FLCE_ERR_WORKSPACE_TOO_SMALL = 2,/* ws_bytes < flce_workspace_bytes(p) */
+  FLCE_ERR_BAD_TARGET = 3,         /* (device) a target outside [0,V) that is not ignore_index */
+  FLCE_ERR_UNSUPPORTED = 4,        /* shape or alignment the kernels do not take (D % 8, 16-B alignment) */
+  FLCE_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
+  FLCE_ERR_TIMEOUT = 6             /* (device) a bounded wait inside a kernel ran out */
+} flce_status;
+
+/* Problem description. Tile and chunk sizes are chosen by the library. */
+typedef struct {
+  int64_t n_rows;        /* N: token rows (>= 0)                           */
+  int64_t hidden;        /* D: hidden size (>= 8, multiple of 8)           */
+  int64_t vocab;         /* V: vocabulary size (>= 1, < 2^31)              */
+  int64_t ignore_index;  /* rows whose target equals this are ignored (-100) */
+  float filter_eps;      /* gradient filter threshold; 0 = off (default).
+                            With eps > 0, a 128-row x 256-column tile of the
+                            unscaled gradient softmax - onehot whose entries
+                            are all below eps in magnitude is left out of dH
+                            and dW (Cut Cross-Entropy, Sec. 4.3 "Gradient
+                            filtering" and Alg. 4; the paper uses 2^-12).    */
+  uint32_t flags;        /* 0, or FLCE_FLAG_* bits below                   */
+} flce_problem;
+
+/* Test hook: every bounded wait inside the GEMM kernels gives up after about
+ * a microsecond, so the timeout path runs and FLCE_ERR_TIMEOUT is recorded.
+ * Outputs are then undefined. */
+#define FLCE_FLAG_TEST_SHORT_WAITS 0x1u
+
+/* Bytes of device workspace the two compute calls need for problem *p
+ * (0 if p is NULL or invalid). Pure host arithmetic; needs no GPU. */
+size_t flce_workspace_bytes(const flce_problem* p);
+
+/* Forward: per-row LSE (all rows, ignored ones included) and the mean loss.
+ *   H    bf16 [N,D]   W bf16 [V,D]   y int64 [N]
+ *   lse  fp32 [N] out (required)     loss fp32 [1] out
+ * Follows "Cut Your Losses in Large-Vocabulary Language Models", Sec. 4.1-4.2
+ * (Alg. 1 and 2), with the loss of the Trillion Labs note. */
+flce_status flce_forward(const flce_problem* p, const void* H, const void* W, const int64_t* y, float* lse,
+                         float* loss, void* ws, size_t ws_bytes, void* stream);
+
+/* Forward and backward in one call, for an upstream gradient grad_loss of the
+ * scalar loss (1 for a plain loss.backward()); gradients are computed in the
+ * same call, as the PyTorch 2.13 chapter describes for scalar reductions
+ * ("scalar reduction에서는 forward가 gradient까지 계산한다").
+ *   lse  fp32 [N] out, or NULL (then kept in ws)   loss fp32 [1] out
+ *   dH   fp32 [N,D] out (overwritten)              dW fp32 [V,D] out (overwritten)
+ * Follows "Cut Your Losses in Large-Vocabulary Language Models", Sec. 4.3 and
+ * Alg. 4, with gradient sign and mean of the Trillion Labs note. */
+flce_status flce_forward_backward(const flce_problem* p, const void* H, const void* W, const int64_t* y,
+                                  float grad_loss, float* lse, float* loss, float* dH, float* dW, void* ws,
+                                  size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns the device status word of the most recent
+ * call that used `ws` (FLCE_OK, FLCE_ERR_BAD_TARGET or FLCE_ERR_TIMEOUT; the
+ * first in that order that is set wins, timeout over bad target) and clears it. */
+flce_status flce_get_device_status(void* ws, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* flce_status_string(flce_status s);
+
+/* Statistic of the most recent flce_forward_backward that used `ws` with
+ * filtering on: the fraction of 128x256 gradient tiles that were skipped.
+ * Synchronises `stream`. Returns 0 when filtering was off. */
+flce_status flce_get_filter_stats(void* ws, void* stream, double* skipped_fraction);
+
+/* Launch timing for profiling. After flce_profile_set(events, kinds, cap),
+ * every kernel the compute calls enqueue is bracketed by two CUDA events
+ * taken from `events` (cudaEvent_t handles created by the caller with timing
+ * enabled): launch i uses events[2i] and events[2i+1], and kinds[i] receives
+ * its FLCE_KERNEL_* code. At most `cap` launches are recorded; later ones
+ * run untimed. flce_profile_set(NULL, NULL, 0) switches recording off.
+ * flce_profile_count returns how many launches were recorded since the last
+ * flce_profile_set. The recording is process-wide and guarded by a mutex;
+ * it adds two event records per launch on the launch stream. */
+#define FLCE_KERNEL_GEMM_LSE 0
+#define FLCE_KERNEL_GEMM_DZ 1
+#define FLCE_KERNEL_GEMM_DW 2
+#define FLCE_KERNEL_GEMM_DH 3
+#define FLCE_KERNEL_PREP 4
+#define FLCE_KERNEL_COMBINE 5
+#define FLCE_KERNEL_FINALIZE 6
+#define FLCE_KERNEL_FILTER_STATS 7
+flce_status flce_profile_set(void** events, int32_t* kinds, int32_t cap);
+int32_t flce_profile_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H_ */

@@ -1,0 +1,187 @@
+"""ctypes binding of include/flce.h: the same entry points, argument marshalling only.
+
+Every function here converts its arguments (torch tensors or raw integer
+addresses, a stream) into the plain pointers and sizes of the C-ABI and
+returns the C status code. Nothing here computes any part of the loss.
+Importing this module loads libflce.so and fails loudly when it is missing.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import re
+
+from .build_lib import INCLUDE, LIB_PATH
+
+HEADER = os.path.join(INCLUDE, "flce.h")
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    ERR_INVALID_ARGUMENT = 1
+    ERR_WORKSPACE_TOO_SMALL = 2
+    ERR_BAD_TARGET = 3
+    ERR_UNSUPPORTED = 4
+    ERR_CUDA = 5
+    ERR_TIMEOUT = 6
+
+
+FLAG_TEST_SHORT_WAITS = 0x1
+
+
+class FlceError(RuntimeError):
+    def __init__(self, status: int, where: str = ""):
+        self.status = Status(status)
+        super().__init__(f"{where}: {self.status.name}" if where else self.status.name)
+
+
+class FlceProblem(ctypes.Structure):
+    _fields_ = [
+        ("n_rows", ctypes.c_int64),
+        ("hidden", ctypes.c_int64),
+        ("vocab", ctypes.c_int64),
+        ("ignore_index", ctypes.c_int64),
+        ("filter_eps", ctypes.c_float),
+        ("flags", ctypes.c_uint32),
+    ]
+
+
+def make_problem(n_rows: int, hidden: int, vocab: int, ignore_index: int = -100,
+                 filter_eps: float = 0.0, flags: int = 0) -> FlceProblem:
+    return FlceProblem(n_rows, hidden, vocab, ignore_index, filter_eps, flags)
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"libflce.so is not built ({LIB_PATH}); build it with lm_head_loss_gb300.build_lib.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, sz, f32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_float
+    prob = ctypes.POINTER(FlceProblem)
+    lib.flce_workspace_bytes.argtypes = [prob]
+    lib.flce_workspace_bytes.restype = sz
+    lib.flce_forward.argtypes = [prob, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.flce_forward.restype = ctypes.c_int
+    lib.flce_forward_backward.argtypes = [prob, vp, vp, vp, f32, vp, vp, vp, vp, vp, sz, vp]
+    lib.flce_forward_backward.restype = ctypes.c_int
+    lib.flce_get_device_status.argtypes = [vp, vp]
+    lib.flce_get_device_status.restype = ctypes.c_int
+    lib.flce_status_string.argtypes = [ctypes.c_int]
+    lib.flce_status_string.restype = ctypes.c_char_p
+    lib.flce_get_filter_stats.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_double)]
+    lib.flce_get_filter_stats.restype = ctypes.c_int
+    lib.flce_profile_set.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]
+    lib.flce_profile_set.restype = ctypes.c_int
+    lib.flce_profile_count.argtypes = []
+    lib.flce_profile_count.restype = ctypes.c_int32
+    return lib
+
+
+lib = _load()
+
+
+def declared_symbols() -> list[str]:
+    """Names of the functions include/flce.h declares."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:size_t|flce_status|int32_t|const char\*)\s+(flce_\w+)\s*\(", text, re.M)))
+
+
+def _addr(x) -> int | None:
+    """Device (or host) address of a tensor, an int, or None for NULL."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _nbytes(ws) -> int:
+    return ws.numel() * ws.element_size()
+
+
+def flce_workspace_bytes(problem: FlceProblem | None) -> int:
+    return int(lib.flce_workspace_bytes(ctypes.byref(problem) if problem is not None else None))
+
+
+def flce_forward(problem, H, W, y, lse, loss, ws, ws_bytes: int | None = None, stream=None) -> Status:
+    nb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    return Status(lib.flce_forward(ctypes.byref(problem) if problem is not None else None, _addr(H), _addr(W),
+                                   _addr(y), _addr(lse), _addr(loss), _addr(ws), nb, _stream(stream)))
+
+
+def flce_forward_backward(problem, H, W, y, grad_loss: float, lse, loss, dH, dW, ws, ws_bytes: int | None = None,
+                          stream=None) -> Status:
+    nb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    return Status(lib.flce_forward_backward(ctypes.byref(problem) if problem is not None else None, _addr(H),
+                                            _addr(W), _addr(y), float(grad_loss), _addr(lse), _addr(loss),
+                                            _addr(dH), _addr(dW), _addr(ws), nb, _stream(stream)))
+
+
+def flce_get_device_status(ws, stream=None) -> Status:
+    return Status(lib.flce_get_device_status(_addr(ws), _stream(stream)))
+
+
+def flce_status_string(status: int) -> str:
+    return lib.flce_status_string(int(status)).decode()
+
+
+def flce_get_filter_stats(ws, stream=None) -> float:
+    out = ctypes.c_double(0.0)
+    st = lib.flce_get_filter_stats(_addr(ws), _stream(stream), ctypes.byref(out))
+    if st != 0:
+        raise FlceError(st, "flce_get_filter_stats")
+    return out.value
+
+
+KERNEL_KINDS = {0: "gemm_lse", 1: "gemm_dz", 2: "gemm_dw", 3: "gemm_dh", 4: "prep", 5: "combine",
+                6: "finalize", 7: "filter_stats"}
+
+
+class LaunchProfiler:
+    """Records CUDA-event pairs around every launch of the library
+    (flce_profile_set); `summary()` gives per-kind launch counts and summed
+    device milliseconds."""
+
+    def __init__(self, capacity: int):
+        import torch
+        self.capacity = capacity
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(2 * capacity)]
+        for e in self.events:           # torch creates the CUDA event on its first record
+            e.record()
+        torch.cuda.synchronize()
+        self._handles = (ctypes.c_void_p * (2 * capacity))(*[e.cuda_event for e in self.events])
+        self._kinds = (ctypes.c_int32 * capacity)()
+
+    def __enter__(self):
+        st = lib.flce_profile_set(self._handles, self._kinds, self.capacity)
+        if st != 0:
+            raise FlceError(st, "flce_profile_set")
+        return self
+
+    def __exit__(self, *exc):
+        self.count = int(lib.flce_profile_count())
+        lib.flce_profile_set(None, None, 0)
+        return False
+
+    def summary(self) -> dict:
+        import torch
+        torch.cuda.synchronize()
+        out: dict = {}
+        for i in range(min(self.count, self.capacity)):
+            kind = KERNEL_KINDS.get(self._kinds[i], str(self._kinds[i]))
+            ms = self.events[2 * i].elapsed_time(self.events[2 * i + 1])
+            d = out.setdefault(kind, {"launches": 0, "ms": 0.0})
+            d["launches"] += 1
+            d["ms"] += ms
+        return out

@@ -1,0 +1,585 @@
+// C-ABI of the fused LM-head cross-entropy (declared in include/flce.h):
+// argument checks, workspace layout, chunk schedule, TMA tensor maps, and the
+// small reduction kernels around the tcgen05 GEMM of tile_gemm.cuh.
+//
+// Schedule of flce_forward_backward (every launch on the caller's stream):
+//   prep                      validate targets, count valid rows, reset status
+//   per row chunk (<= 8192 rows):
+//     GEMM  EPI_LSE           logits tile -> per-tile (max, sum-exp) + target logit
+//     lse_combine             fixed-order merge of the tile partials -> LSE, row losses
+//   finalize                  fixed-order fp64 sum -> mean loss, scale = g / count
+//   per row chunk, per vocabulary chunk (<= 8192 ids):
+//     GEMM  EPI_DZ            recomputed logits -> bf16 G = softmax - onehot -> staging
+//     GEMM  dW chunk          dW[v-chunk] (=|+=) scale * staging^T H[row chunk]
+//     GEMM  dH chunk          dH[row chunk] (=|+=) scale * staging W[v-chunk]
+// The first contribution to an output tile is a plain store and later ones a
+// TMA reduce-add, so no output needs zeroing and every sum runs in launch
+// order: results are bit-reproducible.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "flce.h"
+#include "tile_gemm.cuh"
+
+namespace flce {
+
+constexpr int kRowChunk = 8192;    // rows per chunk (multiple of 256)
+constexpr int kVocabChunk = 8192;  // vocabulary ids per backward chunk (multiple of 256)
+constexpr int kCombineThreads = 256;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr uint64_t kShortWaitNs = 1000ull;
+
+struct alignas(256) WsHeader {
+  uint32_t status;
+  uint32_t filter_on;
+  int64_t count;
+  float scale;
+  float loss;
+  unsigned long long tiles_total;
+  unsigned long long tiles_skipped;
+};
+
+// ------------------------------------------------------------------ kernels
+
+// One block: count targets in [0, V), flag targets that are neither ignored
+// nor in range, reset the status word and the filter statistics.
+__global__ void prep_kernel(const int64_t* __restrict__ y, int64_t n, int64_t vocab, int64_t ignore_index,
+                            uint32_t filter_on, WsHeader* hdr) {
+  __shared__ long long s_cnt[32];
+  __shared__ unsigned s_bad[32];
+  long long cnt = 0;
+  unsigned bad = 0;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const int64_t t = y[i];
+    if (t == ignore_index) continue;
+    if (t >= 0 && t < vocab)
+      ++cnt;
+    else
+      bad = 1u;
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    cnt += __shfl_down_sync(0xffffffffu, cnt, o);
+    bad |= __shfl_down_sync(0xffffffffu, bad, o);
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) {
+    s_cnt[w] = cnt;
+    s_bad[w] = bad;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long c = 0;
+    unsigned b = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+      c += s_cnt[i];
+      b |= s_bad[i];
+    }
+    hdr->count = c;
+    hdr->status = b ? kDevBadTarget : 0u;
+    hdr->filter_on = filter_on;
+    hdr->tiles_total = 0ull;
+    hdr->tiles_skipped = 0ull;
+  }
+}
+
+// One thread per row of a row chunk: merge the per-tile (max, sum) partials
+// in tile order into LSE_n, then sum the row losses of the block in a fixed
+// tree order (fp64).
+__global__ void lse_combine_kernel(const float* __restrict__ part_m, const float* __restrict__ part_s, int part_ld,
+                                   int n_tiles, const float* __restrict__ zy, const int64_t* __restrict__ y,
+                                   int64_t row0, int rows, int64_t vocab, int64_t ignore_index,
+                                   float* __restrict__ lse_out, double* __restrict__ block_sums) {
+  __shared__ double red[kCombineThreads];
+  const int lr = blockIdx.x * kCombineThreads + threadIdx.x;
+  double contrib = 0.0;
+  if (lr < rows) {
+    float mx = -INFINITY, sm = 0.f;
+    for (int t = 0; t < n_tiles; ++t) {
+      const float m = part_m[(size_t)t * part_ld + lr];
+      const float s = part_s[(size_t)t * part_ld + lr];
+      if (m > mx) {
+        sm = sm * exp2f(mx - m) + s;
+        mx = m;
+      } else {
+        sm += s * exp2f(m - mx);
+      }
+    }
+    const float lse = (mx + log2f(sm)) * 0.69314718055994531f;
+    lse_out[row0 + lr] = lse;
+    const int64_t t = y[row0 + lr];
+    if (t != ignore_index && t >= 0 && t < vocab) contrib = (double)lse - (double)zy[lr];
+  }
+  red[threadIdx.x] = contrib;
+  __syncthreads();
+  for (int s = kCombineThreads / 2; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) block_sums[row0 / kCombineThreads + blockIdx.x] = red[0];
+}
+
+// One block: fixed-order fp64 sum of the per-block row losses, mean over the
+// valid count (clamped to one), and the gradient scale g / count.
+__global__ void finalize_kernel(const double* __restrict__ block_sums, int n_blocks, float grad_loss, WsHeader* hdr,
+                                float* loss_out) {
+  __shared__ double red[256];
+  double acc = 0.0;
+  for (int i = threadIdx.x; i < n_blocks; i += 256) acc += block_sums[i];
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double denom = (double)(hdr->count > 0 ? hdr->count : 1);
+    const float loss = (float)(red[0] / denom);
+    hdr->loss = loss;
+    hdr->scale = (float)((double)grad_loss / denom);
+    *loss_out = loss;
+  }
+}
+
+// Filter statistics of one staging chunk: tiles whose flag word is zero were
+// skipped. The chunk's flags occupy rows [0, rows) x columns [0, cols) of a
+// row-major array with leading dimension ld.
+__global__ void count_skipped_kernel(const uint32_t* __restrict__ flags, int rows, int cols, int ld,
+                                     WsHeader* hdr) {
+  __shared__ unsigned red[256];
+  unsigned c = 0;
+  for (int i = threadIdx.x; i < rows * cols; i += 256) c += flags[(size_t)(i / cols) * ld + (i % cols)] == 0u ? 1u : 0u;
+  red[threadIdx.x] = c;
+  __syncthreads();
+  for (int s = 128; s > 0; s >>= 1) {
+    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    atomicAdd(&hdr->tiles_total, (unsigned long long)(rows * cols));
+    atomicAdd(&hdr->tiles_skipped, (unsigned long long)red[0]);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+// Optional launch timing (flce_profile_set): event pairs around every launch.
+struct Profiler {
+  std::mutex mu;
+  void** events = nullptr;
+  int32_t* kinds = nullptr;
+  int32_t cap = 0;
+  int32_t count = 0;
+};
+static Profiler g_prof;
+
+struct ProfScope {
+  cudaStream_t st;
+  int slot = -1;
+  ProfScope(int kind, cudaStream_t s) : st(s) {
+    std::lock_guard<std::mutex> lock(g_prof.mu);
+    if (g_prof.events && g_prof.count < g_prof.cap) {
+      slot = g_prof.count++;
+      g_prof.kinds[slot] = kind;
+      cudaEventRecord(static_cast<cudaEvent_t>(g_prof.events[2 * slot]), st);
+    }
+  }
+  ~ProfScope() {
+    if (slot >= 0) cudaEventRecord(static_cast<cudaEvent_t>(g_prof.events[2 * slot + 1]), st);
+  }
+};
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Plan {
+  int64_t n, d, v;
+  int nc, vc;            // row and vocabulary chunk sizes
+  int n_vtiles;          // ceil(V / 256)
+  int row_chunks, v_chunks;
+  size_t off_pm, off_ps, off_zy, off_lse, off_bsum, off_flags, off_stage, total;
+};
+
+static Plan make_plan(const flce_problem& p) {
+  Plan pl{};
+  pl.n = p.n_rows;
+  pl.d = p.hidden;
+  pl.v = p.vocab;
+  pl.nc = (int)std::min<int64_t>(align_up((size_t)std::max<int64_t>(p.n_rows, 1), 256), kRowChunk);
+  pl.vc = (int)std::min<int64_t>(align_up((size_t)p.vocab, 256), kVocabChunk);
+  pl.n_vtiles = (int)ceil_div(p.vocab, kBN);
+  pl.row_chunks = (int)ceil_div(std::max<int64_t>(p.n_rows, 1), pl.nc);
+  pl.v_chunks = (int)ceil_div(p.vocab, pl.vc);
+  size_t off = align_up(sizeof(WsHeader), 1024);
+  pl.off_pm = off;
+  off = align_up(off + (size_t)pl.n_vtiles * pl.nc * 4, 1024);
+  pl.off_ps = off;
+  off = align_up(off + (size_t)pl.n_vtiles * pl.nc * 4, 1024);
+  pl.off_zy = off;
+  off = align_up(off + (size_t)pl.nc * 4, 1024);
+  pl.off_lse = off;
+  off = align_up(off + (size_t)std::max<int64_t>(p.n_rows, 1) * 4, 1024);
+  pl.off_bsum = off;
+  off = align_up(off + (size_t)pl.row_chunks * (pl.nc / kCombineThreads) * 8, 1024);
+  pl.off_flags = off;
+  off = align_up(off + (size_t)(pl.nc / kBM) * (pl.vc / kBN) * 4, 1024);
+  pl.off_stage = off;
+  off = align_up(off + (size_t)pl.nc * pl.vc * 2, 1024);
+  pl.total = off;
+  return pl;
+}
+
+static bool problem_ok(const flce_problem* p) {
+  if (!p) return false;
+  if (p->n_rows < 0 || p->n_rows > (int64_t)1 << 30) return false;
+  if (p->hidden < 1 || p->hidden > (int64_t)1 << 20) return false;
+  if (p->vocab < 1 || p->vocab >= (int64_t)1 << 31) return false;
+  if (!(p->filter_eps >= 0.f) || !std::isfinite(p->filter_eps)) return false;
+  if ((p->flags & ~FLCE_FLAG_TEST_SHORT_WAITS) != 0u) return false;
+  return true;
+}
+
+static bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor of `outer` rows x `inner` elements, 128-byte swizzle.
+static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+  int sms = 0;
+  bool ready = false;
+};
+
+static bool device_setup(int* sms_out) {
+  static std::mutex mu;
+  static DeviceInfo info[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!info[dev].ready) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    if (cudaFuncSetAttribute(flce_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kGemmSmemBytes) != cudaSuccess)
+      return false;
+    info[dev].sms = sms;
+    info[dev].ready = true;
+  }
+  *sms_out = info[dev].sms;
+  return true;
+}
+
+static bool launch_gemm(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
+                        const GemmParams& gp, int sms, cudaStream_t st) {
+  const int tiles = gp.m_tiles * gp.n_tiles;
+  if (tiles <= 0) return true;
+  const int grid = std::min(tiles, sms);
+  ProfScope prof(kind, st);
+  flce_gemm_kernel<<<grid, kGemmThreads, kGemmSmemBytes, st>>>(a, b, out, gp);
+  return cudaGetLastError() == cudaSuccess;
+}
+
+struct Maps {
+  CUtensorMap h_k, w_k, h_mn, w_mn, s_store, s_k, s_mn, dh, dw;
+};
+
+static GemmParams base_params(const flce_problem& p, WsHeader* hdr) {
+  GemmParams gp;
+  std::memset(&gp, 0, sizeof(gp));
+  gp.ignore_index = p.ignore_index;
+  gp.status = &hdr->status;
+  gp.wait_limit_ns = (p.flags & FLCE_FLAG_TEST_SHORT_WAITS) ? kShortWaitNs : kWaitLimitNs;
+  gp.n_rows = (int32_t)p.n_rows;
+  gp.n_cols = (int32_t)p.vocab;
+  return gp;
+}
+
+// prep + forward GEMM + combine per row chunk + finalize.
+static flce_status run_forward(const flce_problem& p, const Plan& pl, const Maps& mp, const int64_t* y,
+                               float* lse, float* loss, float grad_loss, uint8_t* ws, int sms, cudaStream_t st) {
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  float* part_m = reinterpret_cast<float*>(ws + pl.off_pm);
+  float* part_s = reinterpret_cast<float*>(ws + pl.off_ps);
+  float* zy = reinterpret_cast<float*>(ws + pl.off_zy);
+  double* bsum = reinterpret_cast<double*>(ws + pl.off_bsum);
+  {
+    ProfScope prof(FLCE_KERNEL_PREP, st);
+    prep_kernel<<<1, 1024, 0, st>>>(y, p.n_rows, p.vocab, p.ignore_index, p.filter_eps > 0.f ? 1u : 0u, hdr);
+    if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+  const int k_blocks = (int)ceil_div(p.hidden, kBK);
+  for (int rc = 0; rc < pl.row_chunks && p.n_rows > 0; ++rc) {
+    const int64_t r0 = (int64_t)rc * pl.nc;
+    const int rows = (int)std::min<int64_t>(pl.nc, p.n_rows - r0);
+    GemmParams gp = base_params(p, hdr);
+    gp.m_tiles = (int)ceil_div(rows, kBM);
+    gp.n_tiles = pl.n_vtiles;
+    gp.k_blocks = k_blocks;
+    gp.n_fast = 0;
+    gp.a_m0 = (int32_t)r0;
+    gp.mode = EPI_LSE;
+    gp.m_valid = rows;
+    gp.row0 = (int32_t)r0;
+    gp.col0 = 0;
+    gp.part_ld = pl.nc;
+    gp.part_t0 = 0;
+    gp.y = y;
+    gp.part_m = part_m;
+    gp.part_s = part_s;
+    gp.zy = zy;
+    if (!launch_gemm(FLCE_KERNEL_GEMM_LSE, mp.h_k, mp.w_k, mp.h_k, gp, sms, st)) return FLCE_ERR_CUDA;
+    ProfScope prof(FLCE_KERNEL_COMBINE, st);
+    lse_combine_kernel<<<(int)ceil_div(rows, kCombineThreads), kCombineThreads, 0, st>>>(
+        part_m, part_s, pl.nc, pl.n_vtiles, zy, y, r0, rows, p.vocab, p.ignore_index, lse, bsum);
+    if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+  const int n_blocks = (int)ceil_div(p.n_rows, kCombineThreads);
+  ProfScope prof(FLCE_KERNEL_FINALIZE, st);
+  finalize_kernel<<<1, 256, 0, st>>>(bsum, n_blocks, grad_loss, hdr, loss);
+  if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  return FLCE_OK;
+}
+
+static flce_status run_backward(const flce_problem& p, const Plan& pl, const Maps& mp, const int64_t* y,
+                                const float* lse, uint8_t* ws, int sms, cudaStream_t st) {
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(ws + pl.off_flags);
+  const int filter = p.filter_eps > 0.f ? 1 : 0;
+  const int d_tiles = (int)ceil_div(p.hidden, kBN);
+  for (int rc = 0; rc < pl.row_chunks; ++rc) {
+    const int64_t r0 = (int64_t)rc * pl.nc;
+    const int rows = (int)std::min<int64_t>(pl.nc, p.n_rows - r0);
+    for (int vi = 0; vi < pl.v_chunks; ++vi) {
+      const int64_t v0 = (int64_t)vi * pl.vc;
+      const int cols = (int)std::min<int64_t>(pl.vc, p.vocab - v0);
+      // dZ chunk: recompute logits of rows [r0, r0+rows) x ids [v0, v0+cols).
+      GemmParams dz = base_params(p, hdr);
+      dz.m_tiles = (int)ceil_div(rows, kBM);
+      dz.n_tiles = (int)ceil_div(cols, kBN);
+      dz.k_blocks = (int)ceil_div(p.hidden, kBK);
+      dz.n_fast = 0;
+      dz.a_m0 = (int32_t)r0;
+      dz.b_n0 = (int32_t)v0;
+      dz.mode = EPI_DZ;
+      dz.m_valid = rows;
+      dz.row0 = (int32_t)r0;
+      dz.col0 = (int32_t)v0;
+      dz.y = y;
+      dz.lse = lse;
+      dz.filter = filter;
+      dz.filter_eps = p.filter_eps;
+      dz.flags = flags;
+      dz.flags_ld = pl.vc / kBN;
+      if (!launch_gemm(FLCE_KERNEL_GEMM_DZ, mp.h_k, mp.w_k, mp.s_store, dz, sms, st)) return FLCE_ERR_CUDA;
+      if (filter) {
+        ProfScope prof(FLCE_KERNEL_FILTER_STATS, st);
+        count_skipped_kernel<<<1, 256, 0, st>>>(flags, dz.m_tiles, dz.n_tiles, dz.flags_ld, hdr);
+        if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+      }
+      // dW[v0 : v0+cols, :] (=|+=) scale * staging^T * H[r0 : r0+rows, :]
+      GemmParams dw = base_params(p, hdr);
+      dw.m_tiles = (int)ceil_div(cols, kBM);
+      dw.n_tiles = d_tiles;
+      dw.k_blocks = (int)ceil_div(rows, kBK);
+      dw.a_mn = 1;
+      dw.b_mn = 1;
+      dw.n_fast = 1;
+      dw.b_k0 = (int32_t)r0;
+      dw.mode = rc == 0 ? EPI_STORE : EPI_REDUCE;
+      dw.out_m0 = (int32_t)v0;
+      dw.scale = &hdr->scale;
+      dw.filter = filter;
+      dw.flags = flags;
+      dw.flags_ld = pl.vc / kBN;
+      dw.flags_a_is_rows = 0;
+      if (!launch_gemm(FLCE_KERNEL_GEMM_DW, mp.s_mn, mp.h_mn, mp.dw, dw, sms, st)) return FLCE_ERR_CUDA;
+      // dH[r0 : r0+rows, :] (=|+=) scale * staging * W[v0 : v0+cols, :]
+      GemmParams dh = base_params(p, hdr);
+      dh.m_tiles = (int)ceil_div(rows, kBM);
+      dh.n_tiles = d_tiles;
+      dh.k_blocks = (int)ceil_div(cols, kBK);
+      dh.a_mn = 0;
+      dh.b_mn = 1;
+      dh.n_fast = 1;
+      dh.b_k0 = (int32_t)v0;
+      dh.mode = vi == 0 ? EPI_STORE : EPI_REDUCE;
+      dh.out_m0 = (int32_t)r0;
+      dh.scale = &hdr->scale;
+      dh.filter = filter;
+      dh.flags = flags;
+      dh.flags_ld = pl.vc / kBN;
+      dh.flags_a_is_rows = 1;
+      if (!launch_gemm(FLCE_KERNEL_GEMM_DH, mp.s_k, mp.w_mn, mp.dh, dh, sms, st)) return FLCE_ERR_CUDA;
+    }
+  }
+  return FLCE_OK;
+}
+
+static bool build_maps(const flce_problem& p, const Plan& pl, const void* H, const void* W, float* dH, float* dW,
+                       uint8_t* ws, bool backward, Maps* mp) {
+  const uint64_t D = (uint64_t)p.hidden, N = (uint64_t)std::max<int64_t>(p.n_rows, 1), V = (uint64_t)p.vocab;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  if (!make_map(&mp->h_k, bf, H, D, N, D * 2, 64, kBM)) return false;
+  if (!make_map(&mp->w_k, bf, W, D, V, D * 2, 64, kBN)) return false;
+  if (!backward) return true;
+  void* stage = ws + pl.off_stage;
+  if (!make_map(&mp->h_mn, bf, H, D, N, D * 2, 64, 64)) return false;
+  if (!make_map(&mp->w_mn, bf, W, D, V, D * 2, 64, 64)) return false;
+  if (!make_map(&mp->s_store, bf, stage, (uint64_t)pl.vc, (uint64_t)pl.nc, (uint64_t)pl.vc * 2, 64, 32)) return false;
+  if (!make_map(&mp->s_k, bf, stage, (uint64_t)pl.vc, (uint64_t)pl.nc, (uint64_t)pl.vc * 2, 64, kBM)) return false;
+  if (!make_map(&mp->s_mn, bf, stage, (uint64_t)pl.vc, (uint64_t)pl.nc, (uint64_t)pl.vc * 2, 64, 64)) return false;
+  if (!make_map(&mp->dh, f32, dH, D, N, D * 4, 32, 32)) return false;
+  if (!make_map(&mp->dw, f32, dW, D, V, D * 4, 32, 32)) return false;
+  return true;
+}
+
+static flce_status check_common(const flce_problem* p, const void* H, const void* W, const int64_t* y,
+                                const float* loss, const void* ws, size_t ws_bytes) {
+  if (!problem_ok(p)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!loss || !ws) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->n_rows > 0 && (!H || !y)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!W) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(ws, 256)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(y, 8)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->hidden % 8 != 0) return FLCE_ERR_UNSUPPORTED;
+  if (!aligned(H, 16) || !aligned(W, 16)) return FLCE_ERR_UNSUPPORTED;
+  if (ws_bytes < make_plan(*p).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  return FLCE_OK;
+}
+
+}  // namespace flce
+
+using namespace flce;
+
+extern "C" {
+
+size_t flce_workspace_bytes(const flce_problem* p) {
+  if (!problem_ok(p)) return 0;
+  return make_plan(*p).total;
+}
+
+const char* flce_status_string(flce_status s) {
+  switch (s) {
+    case FLCE_OK: return "FLCE_OK";
+    case FLCE_ERR_INVALID_ARGUMENT: return "FLCE_ERR_INVALID_ARGUMENT";
+    case FLCE_ERR_WORKSPACE_TOO_SMALL: return "FLCE_ERR_WORKSPACE_TOO_SMALL";
+    case FLCE_ERR_BAD_TARGET: return "FLCE_ERR_BAD_TARGET";
+    case FLCE_ERR_UNSUPPORTED: return "FLCE_ERR_UNSUPPORTED";
+    case FLCE_ERR_CUDA: return "FLCE_ERR_CUDA";
+    case FLCE_ERR_TIMEOUT: return "FLCE_ERR_TIMEOUT";
+  }
+  return "FLCE_UNKNOWN_STATUS";
+}
+
+flce_status flce_forward(const flce_problem* p, const void* H, const void* W, const int64_t* y, float* lse,
+                         float* loss, void* ws, size_t ws_bytes, void* stream) {
+  flce_status s = check_common(p, H, W, y, loss, ws, ws_bytes);
+  if (s != FLCE_OK) return s;
+  if (p->n_rows > 0 && !lse) return FLCE_ERR_INVALID_ARGUMENT;
+  int sms = 0;
+  if (!device_setup(&sms)) return FLCE_ERR_CUDA;
+  const Plan pl = make_plan(*p);
+  Maps mp;
+  if (p->n_rows > 0 && !build_maps(*p, pl, H, W, nullptr, nullptr, static_cast<uint8_t*>(ws), false, &mp))
+    return FLCE_ERR_CUDA;
+  return run_forward(*p, pl, mp, y, lse, loss, 1.0f, static_cast<uint8_t*>(ws), sms,
+                     static_cast<cudaStream_t>(stream));
+}
+
+flce_status flce_forward_backward(const flce_problem* p, const void* H, const void* W, const int64_t* y,
+                                  float grad_loss, float* lse, float* loss, float* dH, float* dW, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  flce_status s = check_common(p, H, W, y, loss, ws, ws_bytes);
+  if (s != FLCE_OK) return s;
+  if (!dW || (p->n_rows > 0 && !dH)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(grad_loss)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(dW, 16) || !aligned(dH, 16)) return FLCE_ERR_UNSUPPORTED;
+  int sms = 0;
+  if (!device_setup(&sms)) return FLCE_ERR_CUDA;
+  const Plan pl = make_plan(*p);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* lse_buf = lse ? lse : reinterpret_cast<float*>(wsb + pl.off_lse);
+  if (p->n_rows == 0) {
+    // No rows: loss 0 and dW = 0.
+    Maps none;
+    flce_status r = run_forward(*p, pl, none, y, lse_buf, loss, grad_loss, wsb, sms, st);
+    if (r != FLCE_OK) return r;
+    if (cudaMemsetAsync(dW, 0, (size_t)p->vocab * p->hidden * 4, st) != cudaSuccess) return FLCE_ERR_CUDA;
+    return FLCE_OK;
+  }
+  Maps mp;
+  if (!build_maps(*p, pl, H, W, dH, dW, wsb, true, &mp)) return FLCE_ERR_CUDA;
+  flce_status r = run_forward(*p, pl, mp, y, lse_buf, loss, grad_loss, wsb, sms, st);
+  if (r != FLCE_OK) return r;
+  return run_backward(*p, pl, mp, y, lse_buf, wsb, sms, st);
+}
+
+flce_status flce_get_device_status(void* ws, void* stream) {
+  if (!ws || !aligned(ws, 256)) return FLCE_ERR_INVALID_ARGUMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t status = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (cudaMemcpy(&status, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return FLCE_ERR_CUDA;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(ws, &zero, sizeof(uint32_t), cudaMemcpyHostToDevice) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (status & kDevTimeout) return FLCE_ERR_TIMEOUT;
+  if (status & kDevBadTarget) return FLCE_ERR_BAD_TARGET;
+  return FLCE_OK;
+}
+
+flce_status flce_get_filter_stats(void* ws, void* stream, double* skipped_fraction) {
+  if (!ws || !skipped_fraction || !aligned(ws, 256)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FLCE_ERR_CUDA;
+  WsHeader h;
+  if (cudaMemcpy(&h, ws, sizeof(WsHeader), cudaMemcpyDeviceToHost) != cudaSuccess) return FLCE_ERR_CUDA;
+  *skipped_fraction = (h.filter_on && h.tiles_total) ? (double)h.tiles_skipped / (double)h.tiles_total : 0.0;
+  return FLCE_OK;
+}
+
+flce_status flce_profile_set(void** events, int32_t* kinds, int32_t cap) {
+  if (cap < 0 || (cap > 0 && (!events || !kinds))) return FLCE_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  g_prof.events = cap > 0 ? events : nullptr;
+  g_prof.kinds = cap > 0 ? kinds : nullptr;
+  g_prof.cap = cap;
+  g_prof.count = 0;
+  return FLCE_OK;
+}
+
+int32_t flce_profile_count(void) {
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  return g_prof.count;
+}
+
+}  // extern "C"

@@ -1,0 +1,474 @@
+// Persistent, warp-specialised tcgen05 GEMM with the fused epilogues of the
+// LM-head cross-entropy.
+//
+// One CTA per SM, 192 threads:
+//   warp 0      TMA producer: streams 128x64 A and 256x64 B bf16 tiles
+//               (128-byte swizzle) into a 4-stage shared-memory ring;
+//   warp 1      MMA issuer: one lane issues tcgen05.mma (M=128, N=256, K=16)
+//               into one of two 256-column fp32 TMEM accumulators;
+//   warps 2..5  epilogue: tcgen05.ld the 128x256 accumulator (one thread per
+//               row) and apply one of four epilogues:
+//     EPI_LSE    per-row max and sum of exp over the tile's 256 vocabulary
+//                columns, written as one (max, sum) partial per row and tile,
+//                plus the target logit when the row's target falls in the
+//                tile (the blockwise log-sum-exp of Cut Cross-Entropy,
+//                Sec. 4.2 Alg. 2, fused with the indexed matmul of Alg. 1);
+//     EPI_DZ     G = exp(z - LSE) - onehot(y) for valid rows, 0 otherwise,
+//                rounded to bf16 and stored by TMA into a staging chunk
+//                (Sec. 4.3 Alg. 4, softmax without renormalisation), with an
+//                optional per-tile flag recording whether any |G| >= eps;
+//     EPI_STORE  fp32 tile times a device scalar, stored by TMA;
+//     EPI_REDUCE fp32 tile times a device scalar, added into global memory
+//                by a TMA reduce-add (one writer per element per launch, so
+//                the summation order is fixed by the launch order).
+//
+// The accumulator of tile i lives in TMEM buffer i % 2, so the MMA of the next
+// tile overlaps the epilogue of the current one. Operands may be K-major or
+// MN-major in global memory; both are expressed with 128-byte-swizzled shared
+// memory descriptors, so no operand is ever transposed in memory.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx_sm103.cuh"
+
+namespace flce {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kABytes = kBM * kBK * 2;          // 16 KiB
+constexpr uint32_t kBBytes = kBN * kBK * 2;          // 32 KiB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;  // 48 KiB
+constexpr uint32_t kEpiBoxBytes = 32 * 128;          // 32 rows x 128 bytes
+constexpr uint32_t kEpiBytes = 4 * 2 * kEpiBoxBytes; // 4 warps, double buffered
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kBarrierBytes = 256;
+constexpr uint32_t kGemmSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarrierBytes;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum EpiMode : int32_t { EPI_LSE = 0, EPI_DZ = 1, EPI_STORE = 2, EPI_REDUCE = 3 };
+
+// Device status bits (OR-ed into the workspace status word).
+constexpr uint32_t kDevBadTarget = 1u;
+constexpr uint32_t kDevTimeout = 2u;
+
+struct GemmParams {
+  int32_t m_tiles, n_tiles, k_blocks;
+  int32_t a_mn, b_mn;          // 1 if the operand is MN-major in global memory
+  int32_t n_fast;              // tile raster: 1 = n index varies fastest
+  int32_t a_m0, a_k0;          // coordinate offsets of A (M and K directions)
+  int32_t b_n0, b_k0;          // coordinate offsets of B (N and K directions)
+  int32_t mode;                // EpiMode
+  // epilogue geometry
+  int32_t m_valid;             // local rows >= m_valid are padding
+  int32_t row0;                // global row of local row 0 (LSE / DZ)
+  int32_t n_rows;              // N: global rows >= N are padding
+  int32_t col0;                // global vocabulary id of local column 0 (LSE / DZ)
+  int32_t n_cols;              // V: vocabulary ids >= V are padding (LSE / DZ)
+  int32_t out_m0;              // STORE / REDUCE: row coordinate offset in the output map
+  int32_t part_ld;             // LSE: leading dimension of the partial arrays
+  int32_t part_t0;             // LSE: partial index of n-tile 0
+  int32_t filter;              // DZ: write skip flags; STORE/REDUCE: honour them
+  float filter_eps;
+  int64_t ignore_index;
+  const int64_t* y;
+  const float* lse;            // DZ: natural-log LSE per global row
+  float* part_m;               // LSE: running max (log2 units) [tiles][part_ld]
+  float* part_s;               // LSE: sum of 2^(t - max)       [tiles][part_ld]
+  float* zy;                   // LSE: target logit per local row
+  const float* scale;          // STORE / REDUCE: device scalar multiplier
+  uint32_t* flags;             // per staging tile: 4 quarter flags packed in one word
+  int32_t flags_ld;            // staging tiles per staging row-tile
+  int32_t flags_a_is_rows;     // REDUCE/STORE skip lookup: 1 = K indexes staging columns (dH)
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+};
+
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mt, int& nt) {
+  if (p.n_fast) {
+    nt = t % p.n_tiles;
+    mt = t / p.n_tiles;
+  } else {
+    mt = t % p.m_tiles;
+    nt = t / p.m_tiles;
+  }
+}
+
+// Whether k-block kb of tile (mt, nt) reads only dZ tiles whose gradient was
+// filtered out. Staging tiles are 128 rows x 256 columns.
+//   dH (flags_a_is_rows = 1): A = staging rows mt*128.., columns kb*64..
+//   dW (flags_a_is_rows = 0): A = staging^T, rows kb*64.., columns mt*128..
+__device__ __forceinline__ bool kblock_skipped(const GemmParams& p, int mt, int kb) {
+  if (!p.filter) return false;
+  int srow, scol;
+  if (p.flags_a_is_rows) {
+    srow = mt;
+    scol = (kb * kBK) / kBN;
+  } else {
+    srow = (kb * kBK) / kBM;
+    scol = (mt * kBM) / kBN;
+  }
+  return __ldg(p.flags + (size_t)srow * p.flags_ld + scol) == 0u;
+}
+
+__device__ __forceinline__ void record_timeout(const GemmParams& p, volatile uint32_t* abort_flag) {
+  *abort_flag = 1u;
+  atomicOr(p.status, kDevTimeout);
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* epi_smem = smem + kStages * kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + kEpiBytes);
+  uint64_t* full_bar = bars;                   // [kStages]
+  uint64_t* empty_bar = bars + kStages;        // [kStages]
+  uint64_t* acc_full = bars + 2 * kStages;     // [2]
+  uint64_t* acc_empty = bars + 2 * kStages + 2;// [2]
+  uint64_t* drain_bar = bars + 2 * kStages + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 5);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = p.m_tiles * p.n_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&acc_full[b], 1);
+      ptx::mbar_init(&acc_empty[b], 4);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    ptx::fence_mbarrier_init();
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+    ptx::prefetch_tmap(&tmOut);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int32_t last_parity[kStages];
+      for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(p, t, mt, nt);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (kblock_skipped(p, mt, kb)) continue;
+          if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, p.wait_limit_ns, abort_flag)) {
+            record_timeout(p, abort_flag);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * kStageBytes;
+          uint8_t* sb = sa + kABytes;
+          ptx::mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+          const int32_t kc = kb * kBK;
+          if (p.a_mn) {
+            for (int h = 0; h < kBM / 64; ++h)
+              ptx::tma_load_2d(sa + h * 8192, &tmA, p.a_m0 + mt * kBM + h * 64, p.a_k0 + kc, &full_bar[stage]);
+          } else {
+            ptx::tma_load_2d(sa, &tmA, p.a_k0 + kc, p.a_m0 + mt * kBM, &full_bar[stage]);
+          }
+          if (p.b_mn) {
+            for (int h = 0; h < kBN / 64; ++h)
+              ptx::tma_load_2d(sb + h * 8192, &tmB, p.b_n0 + nt * kBN + h * 64, p.b_k0 + kc, &full_bar[stage]);
+          } else {
+            ptx::tma_load_2d(sb, &tmB, p.b_k0 + kc, p.b_n0 + nt * kBN, &full_bar[stage]);
+          }
+          last_parity[stage] = (int32_t)phase;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Leave no copy in flight into shared memory this CTA is about to give up.
+        volatile uint32_t never = 0u;
+        for (int s = 0; s < kStages; ++s)
+          if (last_parity[s] >= 0) ptx::mbar_wait_bounded(&full_bar[s], (uint32_t)last_parity[s], 100000000ull, &never);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = ptx::idesc_bf16_f32(kBM, kBN, p.a_mn != 0, p.b_mn != 0);
+      const uint32_t smem_base = ptx::smem_u32(smem);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      int i = 0;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++i) {
+        int mt, nt;
+        tile_coords(p, t, mt, nt);
+        const uint32_t buf = i & 1, use = i >> 1;
+        if (!ptx::mbar_wait_bounded(&acc_empty[buf], (use & 1u) ^ 1u, p.wait_limit_ns, abort_flag)) {
+          record_timeout(p, abort_flag);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * kBN;
+        uint32_t accumulate = 0;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (kblock_skipped(p, mt, kb)) continue;
+          if (!ptx::mbar_wait_bounded(&full_bar[stage], phase, p.wait_limit_ns, abort_flag)) {
+            record_timeout(p, abort_flag);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = smem_base + stage * kStageBytes;
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t adesc = p.a_mn ? ptx::smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                          : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
+            const uint64_t bdesc = p.b_mn ? ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                          : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
+            ptx::mma_bf16_ss(d_tmem, adesc, bdesc, idesc, accumulate);
+            accumulate = 1;
+          }
+          ptx::mma_commit(&empty_bar[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&acc_full[buf]);
+      }
+      // Every MMA this thread issued has completed once the drain barrier flips.
+      ptx::mma_commit(drain_bar);
+      volatile uint32_t never = 0u;
+      ptx::mbar_wait_bounded(drain_bar, 0u, 100000000ull, &never);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                    // TMEM lane quarter this warp may read
+    const int r_local = q * 32 + lane;         // row of the tile owned by this thread
+    uint8_t* my_boxes = epi_smem + q * 2 * kEpiBoxBytes;
+    uint32_t ebuf = 0;
+    int i = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++i) {
+      int mt, nt;
+      tile_coords(p, t, mt, nt);
+      const uint32_t buf = i & 1, use = i >> 1;
+      if (!ptx::mbar_wait_bounded(&acc_full[buf], use & 1u, p.wait_limit_ns, abort_flag)) {
+        record_timeout(p, abort_flag);
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem_base + buf * kBN + ((uint32_t)(q * 32) << 16);
+      const int lrow = mt * kBM + r_local;     // local row of this launch
+
+      if (p.mode == EPI_LSE) {
+        const bool in_rows = lrow < p.m_valid && (p.row0 + lrow) < p.n_rows;
+        const int grow = p.row0 + lrow;
+        const int col_t0 = p.col0 + nt * kBN;
+        int yl = -1;
+        if (in_rows) {
+          const int64_t yv = __ldg(p.y + grow);
+          if (yv != p.ignore_index && yv >= 0 && yv < p.n_cols) yl = (int)(yv - col_t0);
+        }
+        const bool ragged = col_t0 + kBN > p.n_cols;
+        float run_max = -INFINITY, run_sum = 0.f, zt = 0.f;
+        bool has_t = false;
+#pragma unroll 1
+        for (int c = 0; c < kBN; c += 32) {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c, r);
+          ptx::tmem_ld_wait();
+          float x[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+          if (ragged) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col_t0 + c + j >= p.n_cols) x[j] = -INFINITY;
+          }
+          if ((unsigned)(yl - c) < 32u) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j == yl - c) zt = x[j];
+            has_t = true;
+          }
+          float cmax = x[0];
+#pragma unroll
+          for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, x[j]);
+          const float new_max = fmaxf(run_max, cmax * kLog2e);
+          float acc = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc += ptx::ex2_approx(fmaf(x[j], kLog2e, -new_max));
+          run_sum = run_sum * ptx::ex2_approx(run_max - new_max) + acc;
+          run_max = new_max;
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
+        if (in_rows) {
+          const size_t idx = (size_t)(p.part_t0 + nt) * p.part_ld + lrow;
+          p.part_m[idx] = run_max;
+          p.part_s[idx] = run_sum;
+          if (has_t) p.zy[lrow] = zt;
+        }
+      } else if (p.mode == EPI_DZ) {
+        const int grow = p.row0 + lrow;
+        const bool in_rows = lrow < p.m_valid && grow < p.n_rows;
+        const int col_t0 = p.col0 + nt * kBN;
+        bool valid = false;
+        int yl = -1;
+        float lse2 = 0.f;
+        if (in_rows) {
+          const int64_t yv = __ldg(p.y + grow);
+          valid = yv != p.ignore_index && yv >= 0 && yv < p.n_cols;
+          if (valid) {
+            yl = (int)(yv - col_t0);
+            lse2 = __ldg(p.lse + grow) * kLog2e;
+          }
+        }
+        const bool ragged = col_t0 + kBN > p.n_cols;
+        float amax = 0.f;
+#pragma unroll 1
+        for (int box = 0; box < kBN / 64; ++box) {
+          uint8_t* sbox = my_boxes + ebuf * kEpiBoxBytes;
+          if (lane == 0) ptx::bulk_wait_group_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int c = box * 64 + half * 32;
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(taddr + c, r);
+            ptx::tmem_ld_wait();
+            float g[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              g[j] = valid ? ptx::ex2_approx(fmaf(__uint_as_float(r[j]), kLog2e, -lse2)) : 0.f;
+            if (ragged) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col_t0 + c + j >= p.n_cols) g[j] = 0.f;
+            }
+            if ((unsigned)(yl - c) < 32u) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j == yl - c) g[j] -= 1.f;
+            }
+            if (p.filter) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(g[j]));
+            }
+            uint32_t packed[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(g[2 * j], g[2 * j + 1]);
+              packed[j] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int chunk = (half * 4 + v) ^ (lane & 7);
+              uint4 val = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+              *reinterpret_cast<uint4*>(sbox + lane * 128 + chunk * 16) = val;
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            ptx::tma_store_2d(&tmOut, sbox, nt * kBN + box * 64, mt * kBM + q * 32);
+            ptx::bulk_commit_group();
+          }
+          ebuf ^= 1u;
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
+        if (p.filter) {
+          // Staging tile (mt, nt) gets one byte per 32-row quarter; the tile
+          // is skipped downstream when the whole 32-bit word is zero.
+          const unsigned keep = __any_sync(0xffffffffu, amax >= p.filter_eps) ? 1u : 0u;
+          if (lane == 0) reinterpret_cast<uint8_t*>(p.flags + (size_t)mt * p.flags_ld + nt)[q] = (uint8_t)keep;
+        }
+      } else {
+        // EPI_STORE / EPI_REDUCE
+        bool all_skipped = p.filter != 0;
+        if (p.filter) {
+          for (int kb = 0; kb < p.k_blocks && all_skipped; ++kb) all_skipped = kblock_skipped(p, mt, kb);
+        }
+        const float sc = __ldg(p.scale);
+        if (!(all_skipped && p.mode == EPI_REDUCE)) {
+#pragma unroll 1
+          for (int c = 0; c < kBN; c += 32) {
+            uint8_t* sbox = my_boxes + ebuf * kEpiBoxBytes;
+            if (lane == 0) ptx::bulk_wait_group_read<1>();
+            __syncwarp();
+            float x[32];
+            if (all_skipped) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) x[j] = 0.f;
+            } else {
+              uint32_t r[32];
+              ptx::tmem_ld_32x32b_x32(taddr + c, r);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * sc;
+            }
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const int chunk = v ^ (lane & 7);
+              *reinterpret_cast<float4*>(sbox + lane * 128 + chunk * 16) =
+                  make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              const int32_t c0 = nt * kBN + c, c1 = p.out_m0 + mt * kBM + q * 32;
+              if (p.mode == EPI_REDUCE)
+                ptx::tma_reduce_add_2d(&tmOut, sbox, c0, c1);
+              else
+                ptx::tma_store_2d(&tmOut, sbox, c0, c1);
+              ptx::bulk_commit_group();
+            }
+            ebuf ^= 1u;
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
+      }
+    }
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
+}
+
+}  // namespace flce

@@ -15,3 +15,15 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def repo_root():
     return ROOT
+
+
+def _ensure_library_built():
+    import importlib.util
+    path = os.path.join(ROOT, "lm_head_loss_gb300", "build_lib.py")
+    spec = importlib.util.spec_from_file_location("_flce_build_lib_conftest", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+
+
+_ensure_library_built()

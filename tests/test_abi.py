@@ -1,0 +1,118 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports every
+symbol include/flce.h declares, sizes its workspace, and rejects bad
+arguments on the host before touching CUDA."""
+
+import ctypes
+import math
+import subprocess
+
+import pytest
+
+import lm_head_loss_gb300 as flce
+from lm_head_loss_gb300 import Status
+from lm_head_loss_gb300.build_lib import LIB_PATH
+
+FAKE = 1 << 20          # a 1 MiB-aligned non-null address: never dereferenced on these paths
+
+
+def test_library_exports_every_declared_symbol():
+    declared = flce.declared_symbols()
+    assert set(declared) == {"flce_workspace_bytes", "flce_forward", "flce_forward_backward",
+                             "flce_get_device_status", "flce_status_string", "flce_get_filter_stats",
+                             "flce_profile_set", "flce_profile_count"}
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared:
+        assert name in exported, name
+        assert hasattr(flce.lib, name)
+
+
+def test_status_strings():
+    for s in Status:
+        assert flce.flce_status_string(s) == "FLCE_" + s.name
+    assert flce.flce_status_string(99) == "FLCE_UNKNOWN_STATUS"
+
+
+def test_workspace_is_linear_in_rows_and_vocab_never_n_times_v():
+    p = flce.make_problem(8192, 2048, 151552)
+    ws = flce.flce_workspace_bytes(p)
+    logits = 8192 * 151552 * 2
+    assert 0 < ws < logits / 10
+    # 16x the rows: O(N) growth only (row chunks reuse the same buffers).
+    p_long = flce.make_problem(131072, 2048, 151552)
+    ws_long = flce.flce_workspace_bytes(p_long)
+    assert ws_long - ws <= 131072 * 4 + (131072 // 256) * 8 + 4096
+    assert ws_long < 131072 * 151552 * 2 / 100
+    # Tiny problems need little.
+    assert flce.flce_workspace_bytes(flce.make_problem(1, 8, 1)) < 1 << 20
+
+
+def test_workspace_bytes_rejects_bad_problems():
+    assert flce.flce_workspace_bytes(None) == 0
+    for args in [(-1, 8, 10), (4, 0, 10), (4, 8, 0), (4, 8, 1 << 31)]:
+        assert flce.flce_workspace_bytes(flce.make_problem(*args)) == 0
+    assert flce.flce_workspace_bytes(flce.make_problem(4, 8, 10, filter_eps=-1.0)) == 0
+    assert flce.flce_workspace_bytes(flce.make_problem(4, 8, 10, filter_eps=math.inf)) == 0
+    assert flce.flce_workspace_bytes(flce.make_problem(4, 8, 10, flags=0x80)) == 0
+    assert flce.flce_workspace_bytes(flce.make_problem(0, 8, 10)) > 0
+
+
+def _fwd(prob, H=FAKE, W=FAKE, y=FAKE, lse=FAKE, loss=FAKE, ws=FAKE, nb=None):
+    nb = flce.flce_workspace_bytes(prob) if nb is None and prob is not None else (nb or 0)
+    return flce.flce_forward(prob, H, W, y, lse, loss, ws, ws_bytes=nb, stream=0)
+
+
+def _fb(prob, H=FAKE, W=FAKE, y=FAKE, lse=None, loss=FAKE, dH=FAKE, dW=FAKE, ws=FAKE, nb=None, g=1.0):
+    nb = flce.flce_workspace_bytes(prob) if nb is None and prob is not None else (nb or 0)
+    return flce.flce_forward_backward(prob, H, W, y, g, lse, loss, dH, dW, ws, ws_bytes=nb, stream=0)
+
+
+def test_host_argument_checks_return_before_any_launch():
+    good = flce.make_problem(16, 64, 100)
+    assert _fwd(None) == Status.ERR_INVALID_ARGUMENT
+    assert _fwd(good, H=None) == Status.ERR_INVALID_ARGUMENT
+    assert _fwd(good, W=None) == Status.ERR_INVALID_ARGUMENT
+    assert _fwd(good, y=None) == Status.ERR_INVALID_ARGUMENT
+    assert _fwd(good, lse=None) == Status.ERR_INVALID_ARGUMENT
+    assert _fwd(good, loss=None) == Status.ERR_INVALID_ARGUMENT
+    assert _fwd(good, ws=None) == Status.ERR_INVALID_ARGUMENT
+    assert _fwd(good, ws=FAKE + 16) == Status.ERR_INVALID_ARGUMENT          # ws not 256-byte aligned
+    assert _fwd(good, y=FAKE + 4) == Status.ERR_INVALID_ARGUMENT            # int64 targets misaligned
+    assert _fwd(good, H=FAKE + 8) == Status.ERR_UNSUPPORTED                 # TMA needs 16-byte alignment
+    assert _fwd(good, nb=flce.flce_workspace_bytes(good) - 1) == Status.ERR_WORKSPACE_TOO_SMALL
+    assert _fwd(flce.make_problem(16, 60, 100)) == Status.ERR_UNSUPPORTED   # D % 8 != 0
+    assert _fwd(flce.make_problem(16, 64, 100, flags=0x4)) == Status.ERR_INVALID_ARGUMENT
+    assert _fwd(flce.make_problem(16, 64, 100, filter_eps=float("nan"))) == Status.ERR_INVALID_ARGUMENT
+    assert _fb(good, dW=None) == Status.ERR_INVALID_ARGUMENT
+    assert _fb(good, dH=None) == Status.ERR_INVALID_ARGUMENT
+    assert _fb(good, dH=FAKE + 4) == Status.ERR_UNSUPPORTED
+    assert _fb(good, g=float("inf")) == Status.ERR_INVALID_ARGUMENT
+    assert _fb(good, nb=1) == Status.ERR_WORKSPACE_TOO_SMALL
+
+
+def test_profile_hook_arguments():
+    assert flce.lib.flce_profile_set(None, None, -1) == Status.ERR_INVALID_ARGUMENT
+    assert flce.lib.flce_profile_set(None, None, 4) == Status.ERR_INVALID_ARGUMENT
+    assert flce.lib.flce_profile_set(None, None, 0) == Status.OK
+    assert flce.lib.flce_profile_count() == 0
+
+
+def test_device_status_rejects_null_workspace():
+    assert flce.flce_get_device_status(None, stream=0) == Status.ERR_INVALID_ARGUMENT
+    with pytest.raises(flce.FlceError):
+        flce.flce_get_filter_stats(None, stream=0)
+
+
+def test_problem_struct_layout_matches_header():
+    # int64 x4, float, uint32 -> 40 bytes, 8-byte aligned.
+    assert ctypes.sizeof(flce.FlceProblem) == 40
+    assert flce.FlceProblem.filter_eps.offset == 32 and flce.FlceProblem.flags.offset == 36
+
+
+def test_api_refuses_cpu_tensors():
+    import torch
+    H = torch.zeros(4, 8, dtype=torch.bfloat16)
+    W = torch.zeros(5, 8, dtype=torch.bfloat16)
+    y = torch.zeros(4, dtype=torch.int64)
+    with pytest.raises(ValueError):
+        flce.forward(H, W, y)

@@ -1,0 +1,129 @@
+"""GPU parity at the full workload sizes, in the launch configuration the
+benchmark times (one flce_forward_backward call on the whole batch).
+
+At 8192 rows the oracle runs its full fp64 forward (every LSE and the loss);
+dH and dW are compared on seeded samples of rows and vocabulary ids that the
+oracle computes one by one. At 131072 rows the forward is sampled too, and
+the loss and dW are checked through identities that hold at any size:
+loss = mean over valid rows of (LSE_n - z_{n,y_n}); sum_v dW_v = 0;
+<W, dW> = <H, dH>.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import lm_head_loss_gb300 as flce
+import oracle
+import synth
+from gpu_common import GRAD_REL, LOSS_REL, LSE_ABS, to_device
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+N_SAMPLE_ROWS = 256
+N_SAMPLE_VOCAB = 256
+
+
+def _run(inp, filter_eps=0.0):
+    H, W, y = to_device(inp)
+    ws = flce.Workspace(H.device)
+    loss, lse, dH, dW = flce.forward_backward(H, W, y, workspace=ws, filter_eps=filter_eps)
+    st = flce.device_status(ws)
+    out = {"loss": loss.item(), "lse": lse.cpu().numpy(), "dH": dH.cpu().numpy(), "dW": dW.cpu().numpy(),
+           "status": st}
+    if filter_eps > 0:
+        out["skipped"] = flce.flce_get_filter_stats(ws.buf)
+    del H, W, y, ws, lse, dH, dW
+    torch.cuda.empty_cache()
+    return out
+
+
+def _samples(inp, seed):
+    rng = np.random.default_rng(seed)
+    n, v = inp["H"].shape[0], inp["W"].shape[0]
+    rows = np.sort(rng.choice(n, size=min(N_SAMPLE_ROWS, n), replace=False))
+    y = inp["y"]
+    frequent = np.bincount(y[y >= 0], minlength=v).argsort()[::-1][:32]
+    vocab = np.unique(np.concatenate([frequent, rng.choice(v, size=N_SAMPLE_VOCAB - 32, replace=False),
+                                      [v - 1]]))
+    return rows, vocab
+
+
+def _check_sampled(inp, got, full_forward: bool, seed=0):
+    H64, W64 = oracle.inputs_f64(inp["H"], inp["W"])
+    y = inp["y"]
+    rows, vocab = _samples(inp, seed)
+    report = {}
+    if full_forward:
+        lse, loss, _ = oracle.forward(H64, W64, y)
+        report["lse_abs"] = float(np.max(np.abs(got["lse"] - lse)))
+        report["loss_rel"] = abs(got["loss"] - loss) / abs(loss)
+        dW_ref = oracle.dW_rows(H64, W64, y, lse, vocab)
+        report["dW_rel_sampled"] = float(np.max(np.abs(got["dW"][vocab] - dW_ref)) / np.max(np.abs(dW_ref)))
+    else:
+        lse_s = oracle.lse_rows(H64, W64, rows)
+        report["lse_abs_sampled"] = float(np.max(np.abs(got["lse"][rows] - lse_s)))
+        valid = y != -100
+        zy = np.einsum("nd,nd->n", H64[valid], W64[y[valid]])
+        loss_from_lse = float(np.sum(got["lse"][valid].astype(np.float64) - zy) / max(valid.sum(), 1))
+        report["loss_rel_given_lse"] = abs(got["loss"] - loss_from_lse) / abs(loss_from_lse)
+    dH_ref = oracle.dH_rows(H64, W64, y, rows)
+    report["dH_rel_sampled"] = float(np.max(np.abs(got["dH"][rows] - dH_ref)) / np.max(np.abs(dH_ref)))
+    dW64 = got["dW"].astype(np.float64)
+    dH64 = got["dH"].astype(np.float64)
+    report["dW_colsum_rel"] = float(np.max(np.abs(dW64.sum(axis=0))) / np.max(np.abs(dW64)))
+    a, b = float(np.sum(W64 * dW64)), float(np.sum(H64 * dH64))
+    report["inner_product_rel"] = abs(a - b) / max(abs(a), abs(b))
+    return report
+
+
+def _assert_report(r):
+    for k, v in r.items():
+        if k.startswith("lse_abs"):
+            assert v <= LSE_ABS, r
+        elif k.startswith("loss_rel"):
+            assert v <= LOSS_REL, r
+        else:
+            assert v <= GRAD_REL, r
+
+
+@pytest.mark.parametrize("name", ["gravity16b_head", "llama3_8b_head"])
+def test_full_size_8192_rows(name):
+    inp = synth.make_inputs(synth.WORKLOADS[name], seed=0)
+    got = _run(inp)
+    assert got["status"] == flce.Status.OK
+    r = _check_sampled(inp, got, full_forward=True)
+    print(name, r)
+    _assert_report(r)
+
+
+def test_full_size_gemma_filter_off_and_on():
+    inp = synth.make_inputs(synth.WORKLOADS["gemma2_2b_head"], seed=0)
+    off = _run(inp)
+    assert off["status"] == flce.Status.OK
+    r = _check_sampled(inp, off, full_forward=True)
+    print("gemma filter off", r)
+    _assert_report(r)
+    on = _run(inp, filter_eps=2.0 ** -12)
+    # The filtered variant is reported against the unfiltered oracle, not gated
+    # by the filter-off tolerances: it drops tiles whose every |G| < 2^-12.
+    r_on = _check_sampled(inp, on, full_forward=True)
+    print("gemma filter on", r_on, "skipped tile fraction", on["skipped"])
+    assert on["loss"] == off["loss"]
+    assert r_on["dH_rel_sampled"] <= 5e-2 and r_on["dW_rel_sampled"] <= 5e-2
+
+
+def test_full_size_long_context_131072_rows():
+    inp = synth.make_inputs(synth.WORKLOADS["long128k_head"], seed=0)
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    got = _run(inp)
+    peak = torch.cuda.max_memory_allocated() - base
+    assert got["status"] == flce.Status.OK
+    # Inputs + outputs + workspace, far below the 37 GiB of bf16 logits.
+    wl = synth.WORKLOADS["long128k_head"]
+    assert peak < wl.logits_bytes_bf16() / 4
+    r = _check_sampled(inp, got, full_forward=False)
+    print("long128k", r, "peak MiB", peak / 2 ** 20)
+    _assert_report(r)
