@@ -61,6 +61,27 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Maximum of a per-rank scalar over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_throughput(rows_per_rank: int, world: int, steps: int, max_total_ms: float) -> float:
+    """Rows processed by all ranks per second, timed by the slowest rank."""
+    return rows_per_rank * world * steps / (max_total_ms / 1e3)
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own batch (independent problems, weak scaling)."""
+    return base_seed + rank
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -168,7 +189,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = synth.WORKLOADS[args.workload]
-    inp = synth.make_inputs(wl, seed=args.seed + rank)
+    inp = synth.make_inputs(wl, seed=rank_seed(args.seed, rank))
     N, D, V = wl.n_rows, wl.hidden, wl.vocab
     H = torch.from_numpy(inp["H"].view(np.int16)).view(torch.bfloat16).to(dev)
     W = torch.from_numpy(inp["W"].view(np.int16)).view(torch.bfloat16).to(dev)
@@ -226,12 +247,9 @@ def run_ours(args, rank, world, local):
     per_kind = prof.summary()
     clk = clocks.summary()
 
-    ms_t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    total_ms_max = float(ms_t.item())
+    total_ms_max = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms_max / args.steps
-    value = N * world * args.steps / (total_ms_max / 1e3)
+    value = weak_scaling_throughput(N, world, args.steps, total_ms_max)
 
     flops_step = 8.0 * N * V * D
     peaks, peak_src = measured_peaks()
@@ -308,13 +326,11 @@ def run_e2e(args, flce, torch, inp, prob, ws, outs, dev, stream, world, dist):
         step()
     end.record(stream)
     torch.cuda.synchronize()
-    ms = torch.tensor([start.elapsed_time(end)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+    ms = max_over_ranks(start.elapsed_time(end), world, dev)
     n = inp["H"].shape[0]
-    return {"value": n * world * args.steps / (float(ms.item()) / 1e3), "unit": UNIT,
+    return {"value": weak_scaling_throughput(n, world, args.steps, ms), "unit": UNIT,
             "h2d_bytes_per_step": int(hH.numel() * 2 + hW.numel() * 2 + hy.numel() * 8),
-            "d2h_bytes_per_step": 4, "ms_per_step": float(ms.item()) / args.steps}
+            "d2h_bytes_per_step": 4, "ms_per_step": ms / args.steps}
 
 
 # ------------------------------------------------------------------ reference arm

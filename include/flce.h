@@ -131,12 +131,13 @@ flce_status flce_get_filter_stats(void* ws, void* stream, double* skipped_fracti
  * it adds two event records per launch on the launch stream. */
 #define FLCE_KERNEL_GEMM_LSE 0
 #define FLCE_KERNEL_GEMM_DZ 1
-#define FLCE_KERNEL_GEMM_DW 2
-#define FLCE_KERNEL_GEMM_DH 3
+#define FLCE_KERNEL_GEMM_DW 2 /* reserved: dW runs inside FLCE_KERNEL_GEMM_BWD launches */
+#define FLCE_KERNEL_GEMM_DH 3 /* reserved: dH runs inside FLCE_KERNEL_GEMM_BWD launches */
 #define FLCE_KERNEL_PREP 4
 #define FLCE_KERNEL_COMBINE 5
 #define FLCE_KERNEL_FINALIZE 6
 #define FLCE_KERNEL_FILTER_STATS 7
+#define FLCE_KERNEL_GEMM_BWD 8 /* one launch: dW and dH of a chunk + dZ of the next chunk */
 flce_status flce_profile_set(void** events, int32_t* kinds, int32_t cap);
 int32_t flce_profile_count(void);
 

@@ -145,7 +145,7 @@ def flce_get_filter_stats(ws, stream=None) -> float:
 
 
 KERNEL_KINDS = {0: "gemm_lse", 1: "gemm_dz", 2: "gemm_dw", 3: "gemm_dh", 4: "prep", 5: "combine",
-                6: "finalize", 7: "filter_stats"}
+                6: "finalize", 7: "filter_stats", 8: "gemm_bwd"}
 
 
 class LaunchProfiler:

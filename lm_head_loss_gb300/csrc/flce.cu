@@ -203,7 +203,7 @@ struct Plan {
   int nc, vc;            // row and vocabulary chunk sizes
   int n_vtiles;          // ceil(V / 256)
   int row_chunks, v_chunks;
-  size_t off_pm, off_ps, off_zy, off_lse, off_bsum, off_flags, off_stage, total;
+  size_t off_pm, off_ps, off_zy, off_lse, off_bsum, off_flags[2], off_stage[2], total;
 };
 
 static Plan make_plan(const flce_problem& p) {
@@ -227,10 +227,14 @@ static Plan make_plan(const flce_problem& p) {
   off = align_up(off + (size_t)std::max<int64_t>(p.n_rows, 1) * 4, 1024);
   pl.off_bsum = off;
   off = align_up(off + (size_t)pl.row_chunks * (pl.nc / kCombineThreads) * 8, 1024);
-  pl.off_flags = off;
-  off = align_up(off + (size_t)(pl.nc / kBM) * (pl.vc / kBN) * 4, 1024);
-  pl.off_stage = off;
-  off = align_up(off + (size_t)pl.nc * pl.vc * 2, 1024);
+  for (int b = 0; b < 2; ++b) {
+    pl.off_flags[b] = off;
+    off = align_up(off + (size_t)(pl.nc / kBM) * (pl.vc / kBN) * 4, 1024);
+  }
+  for (int b = 0; b < 2; ++b) {
+    pl.off_stage[b] = off;
+    off = align_up(off + (size_t)pl.nc * pl.vc * 2, 1024);
+  }
   pl.total = off;
   return pl;
 }
@@ -299,18 +303,35 @@ static bool device_setup(int* sms_out) {
   return true;
 }
 
-static bool launch_gemm(int kind, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out,
-                        const GemmParams& gp, int sms, cudaStream_t st) {
-  const int tiles = gp.m_tiles * gp.n_tiles;
-  if (tiles <= 0) return true;
-  const int grid = std::min(tiles, sms);
+// Collects up to kMaxProblems GEMM problems for one persistent launch.
+struct Group {
+  GemmLaunch L;
+  int tiles = 0;
+  Group() { std::memset(&L, 0, sizeof(L)); }
+  void add(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, const GemmParams& gp) {
+    const int t = gp.m_tiles * gp.n_tiles;
+    if (t <= 0) return;
+    const int q = L.n_probs++;
+    L.tm_a[q] = a;
+    L.tm_b[q] = b;
+    L.tm_out[q] = out;
+    L.prob[q] = gp;
+    tiles += t;
+    L.tile_end[q] = tiles;
+  }
+};
+
+static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
+  if (g.tiles <= 0) return true;
+  const int grid = std::min(g.tiles, sms);
   ProfScope prof(kind, st);
-  flce_gemm_kernel<<<grid, kGemmThreads, kGemmSmemBytes, st>>>(a, b, out, gp);
+  flce_gemm_kernel<<<grid, kGemmThreads, kGemmSmemBytes, st>>>(g.L);
   return cudaGetLastError() == cudaSuccess;
 }
 
 struct Maps {
-  CUtensorMap h_k, w_k, h_mn, w_mn, s_store, s_k, s_mn, dh, dw;
+  CUtensorMap h_k, w_k, h_mn, w_mn, dh, dw;
+  CUtensorMap s_store[2], s_k[2], s_mn[2];   // one set per staging buffer
 };
 
 static GemmParams base_params(const flce_problem& p, WsHeader* hdr) {
@@ -357,7 +378,9 @@ static flce_status run_forward(const flce_problem& p, const Plan& pl, const Maps
     gp.part_m = part_m;
     gp.part_s = part_s;
     gp.zy = zy;
-    if (!launch_gemm(FLCE_KERNEL_GEMM_LSE, mp.h_k, mp.w_k, mp.h_k, gp, sms, st)) return FLCE_ERR_CUDA;
+    Group g;
+    g.add(mp.h_k, mp.w_k, mp.h_k, gp);
+    if (!launch_group(FLCE_KERNEL_GEMM_LSE, g, sms, st)) return FLCE_ERR_CUDA;
     ProfScope prof(FLCE_KERNEL_COMBINE, st);
     lse_combine_kernel<<<(int)ceil_div(rows, kCombineThreads), kCombineThreads, 0, st>>>(
         part_m, part_s, pl.nc, pl.n_vtiles, zy, y, r0, rows, p.vocab, p.ignore_index, lse, bsum);
@@ -370,77 +393,109 @@ static flce_status run_forward(const flce_problem& p, const Plan& pl, const Maps
   return FLCE_OK;
 }
 
+// The backward walks (row chunk, vocabulary chunk) items in order. Item s
+// stages its dZ in buffer s % 2. The dZ GEMM of item s+1 shares a launch with
+// the dW and dH GEMMs of item s: they touch different staging buffers.
 static flce_status run_backward(const flce_problem& p, const Plan& pl, const Maps& mp, const int64_t* y,
                                 const float* lse, uint8_t* ws, int sms, cudaStream_t st) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
-  uint32_t* flags = reinterpret_cast<uint32_t*>(ws + pl.off_flags);
   const int filter = p.filter_eps > 0.f ? 1 : 0;
   const int d_tiles = (int)ceil_div(p.hidden, kBN);
-  for (int rc = 0; rc < pl.row_chunks; ++rc) {
-    const int64_t r0 = (int64_t)rc * pl.nc;
-    const int rows = (int)std::min<int64_t>(pl.nc, p.n_rows - r0);
-    for (int vi = 0; vi < pl.v_chunks; ++vi) {
-      const int64_t v0 = (int64_t)vi * pl.vc;
-      const int cols = (int)std::min<int64_t>(pl.vc, p.vocab - v0);
-      // dZ chunk: recompute logits of rows [r0, r0+rows) x ids [v0, v0+cols).
-      GemmParams dz = base_params(p, hdr);
-      dz.m_tiles = (int)ceil_div(rows, kBM);
-      dz.n_tiles = (int)ceil_div(cols, kBN);
-      dz.k_blocks = (int)ceil_div(p.hidden, kBK);
-      dz.n_fast = 0;
-      dz.a_m0 = (int32_t)r0;
-      dz.b_n0 = (int32_t)v0;
-      dz.mode = EPI_DZ;
-      dz.m_valid = rows;
-      dz.row0 = (int32_t)r0;
-      dz.col0 = (int32_t)v0;
-      dz.y = y;
-      dz.lse = lse;
-      dz.filter = filter;
-      dz.filter_eps = p.filter_eps;
-      dz.flags = flags;
-      dz.flags_ld = pl.vc / kBN;
-      if (!launch_gemm(FLCE_KERNEL_GEMM_DZ, mp.h_k, mp.w_k, mp.s_store, dz, sms, st)) return FLCE_ERR_CUDA;
-      if (filter) {
-        ProfScope prof(FLCE_KERNEL_FILTER_STATS, st);
-        count_skipped_kernel<<<1, 256, 0, st>>>(flags, dz.m_tiles, dz.n_tiles, dz.flags_ld, hdr);
-        if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
-      }
-      // dW[v0 : v0+cols, :] (=|+=) scale * staging^T * H[r0 : r0+rows, :]
-      GemmParams dw = base_params(p, hdr);
-      dw.m_tiles = (int)ceil_div(cols, kBM);
-      dw.n_tiles = d_tiles;
-      dw.k_blocks = (int)ceil_div(rows, kBK);
-      dw.a_mn = 1;
-      dw.b_mn = 1;
-      dw.n_fast = 1;
-      dw.b_k0 = (int32_t)r0;
-      dw.mode = rc == 0 ? EPI_STORE : EPI_REDUCE;
-      dw.out_m0 = (int32_t)v0;
-      dw.scale = &hdr->scale;
-      dw.filter = filter;
-      dw.flags = flags;
-      dw.flags_ld = pl.vc / kBN;
-      dw.flags_a_is_rows = 0;
-      if (!launch_gemm(FLCE_KERNEL_GEMM_DW, mp.s_mn, mp.h_mn, mp.dw, dw, sms, st)) return FLCE_ERR_CUDA;
-      // dH[r0 : r0+rows, :] (=|+=) scale * staging * W[v0 : v0+cols, :]
-      GemmParams dh = base_params(p, hdr);
-      dh.m_tiles = (int)ceil_div(rows, kBM);
-      dh.n_tiles = d_tiles;
-      dh.k_blocks = (int)ceil_div(cols, kBK);
-      dh.a_mn = 0;
-      dh.b_mn = 1;
-      dh.n_fast = 1;
-      dh.b_k0 = (int32_t)v0;
-      dh.mode = vi == 0 ? EPI_STORE : EPI_REDUCE;
-      dh.out_m0 = (int32_t)r0;
-      dh.scale = &hdr->scale;
-      dh.filter = filter;
-      dh.flags = flags;
-      dh.flags_ld = pl.vc / kBN;
-      dh.flags_a_is_rows = 1;
-      if (!launch_gemm(FLCE_KERNEL_GEMM_DH, mp.s_k, mp.w_mn, mp.dh, dh, sms, st)) return FLCE_ERR_CUDA;
+  const int items = pl.row_chunks * pl.v_chunks;
+  auto item_geom = [&](int s, int64_t& r0, int& rows, int64_t& v0, int& cols) {
+    const int rc = s / pl.v_chunks, vi = s % pl.v_chunks;
+    r0 = (int64_t)rc * pl.nc;
+    rows = (int)std::min<int64_t>(pl.nc, p.n_rows - r0);
+    v0 = (int64_t)vi * pl.vc;
+    cols = (int)std::min<int64_t>(pl.vc, p.vocab - v0);
+  };
+  auto dz_params = [&](int s) {
+    int64_t r0, v0;
+    int rows, cols;
+    item_geom(s, r0, rows, v0, cols);
+    GemmParams dz = base_params(p, hdr);
+    dz.m_tiles = (int)ceil_div(rows, kBM);
+    dz.n_tiles = (int)ceil_div(cols, kBN);
+    dz.k_blocks = (int)ceil_div(p.hidden, kBK);
+    dz.n_fast = 0;
+    dz.a_m0 = (int32_t)r0;
+    dz.b_n0 = (int32_t)v0;
+    dz.mode = EPI_DZ;
+    dz.m_valid = rows;
+    dz.row0 = (int32_t)r0;
+    dz.col0 = (int32_t)v0;
+    dz.y = y;
+    dz.lse = lse;
+    dz.filter = filter;
+    dz.filter_eps = p.filter_eps;
+    dz.flags = reinterpret_cast<uint32_t*>(ws + pl.off_flags[s & 1]);
+    dz.flags_ld = pl.vc / kBN;
+    return dz;
+  };
+  auto count_skipped = [&](const GemmParams& dz) -> bool {
+    if (!filter) return true;
+    ProfScope prof(FLCE_KERNEL_FILTER_STATS, st);
+    count_skipped_kernel<<<1, 256, 0, st>>>(dz.flags, dz.m_tiles, dz.n_tiles, dz.flags_ld, hdr);
+    return cudaGetLastError() == cudaSuccess;
+  };
+
+  {
+    Group g;
+    const GemmParams dz0 = dz_params(0);
+    g.add(mp.h_k, mp.w_k, mp.s_store[0], dz0);
+    if (!launch_group(FLCE_KERNEL_GEMM_DZ, g, sms, st)) return FLCE_ERR_CUDA;
+    if (!count_skipped(dz0)) return FLCE_ERR_CUDA;
+  }
+  for (int s = 0; s < items; ++s) {
+    const int b = s & 1;
+    int64_t r0, v0;
+    int rows, cols;
+    item_geom(s, r0, rows, v0, cols);
+    const int rc = s / pl.v_chunks, vi = s % pl.v_chunks;
+    uint32_t* flags = reinterpret_cast<uint32_t*>(ws + pl.off_flags[b]);
+    Group g;
+    // dW[v0 : v0+cols, :] (=|+=) scale * staging^T * H[r0 : r0+rows, :]
+    GemmParams dw = base_params(p, hdr);
+    dw.m_tiles = (int)ceil_div(cols, kBM);
+    dw.n_tiles = d_tiles;
+    dw.k_blocks = (int)ceil_div(rows, kBK);
+    dw.a_mn = 1;
+    dw.b_mn = 1;
+    dw.n_fast = 1;
+    dw.b_k0 = (int32_t)r0;
+    dw.mode = rc == 0 ? EPI_STORE : EPI_REDUCE;
+    dw.out_m0 = (int32_t)v0;
+    dw.scale = &hdr->scale;
+    dw.filter = filter;
+    dw.flags = flags;
+    dw.flags_ld = pl.vc / kBN;
+    dw.flags_a_is_rows = 0;
+    g.add(mp.s_mn[b], mp.h_mn, mp.dw, dw);
+    // dH[r0 : r0+rows, :] (=|+=) scale * staging * W[v0 : v0+cols, :]
+    GemmParams dh = base_params(p, hdr);
+    dh.m_tiles = (int)ceil_div(rows, kBM);
+    dh.n_tiles = d_tiles;
+    dh.k_blocks = (int)ceil_div(cols, kBK);
+    dh.a_mn = 0;
+    dh.b_mn = 1;
+    dh.n_fast = 1;
+    dh.b_k0 = (int32_t)v0;
+    dh.mode = vi == 0 ? EPI_STORE : EPI_REDUCE;
+    dh.out_m0 = (int32_t)r0;
+    dh.scale = &hdr->scale;
+    dh.filter = filter;
+    dh.flags = flags;
+    dh.flags_ld = pl.vc / kBN;
+    dh.flags_a_is_rows = 1;
+    g.add(mp.s_k[b], mp.w_mn, mp.dh, dh);
+    GemmParams dz_next;
+    const bool has_next = s + 1 < items;
+    if (has_next) {
+      dz_next = dz_params(s + 1);
+      g.add(mp.h_k, mp.w_k, mp.s_store[b ^ 1], dz_next);
     }
+    if (!launch_group(FLCE_KERNEL_GEMM_BWD, g, sms, st)) return FLCE_ERR_CUDA;
+    if (has_next && !count_skipped(dz_next)) return FLCE_ERR_CUDA;
   }
   return FLCE_OK;
 }
@@ -452,12 +507,15 @@ static bool build_maps(const flce_problem& p, const Plan& pl, const void* H, con
   if (!make_map(&mp->h_k, bf, H, D, N, D * 2, 64, kBM)) return false;
   if (!make_map(&mp->w_k, bf, W, D, V, D * 2, 64, kBN)) return false;
   if (!backward) return true;
-  void* stage = ws + pl.off_stage;
   if (!make_map(&mp->h_mn, bf, H, D, N, D * 2, 64, 64)) return false;
   if (!make_map(&mp->w_mn, bf, W, D, V, D * 2, 64, 64)) return false;
-  if (!make_map(&mp->s_store, bf, stage, (uint64_t)pl.vc, (uint64_t)pl.nc, (uint64_t)pl.vc * 2, 64, 32)) return false;
-  if (!make_map(&mp->s_k, bf, stage, (uint64_t)pl.vc, (uint64_t)pl.nc, (uint64_t)pl.vc * 2, 64, kBM)) return false;
-  if (!make_map(&mp->s_mn, bf, stage, (uint64_t)pl.vc, (uint64_t)pl.nc, (uint64_t)pl.vc * 2, 64, 64)) return false;
+  for (int b = 0; b < 2; ++b) {
+    void* stage = ws + pl.off_stage[b];
+    const uint64_t vc = (uint64_t)pl.vc, nc = (uint64_t)pl.nc;
+    if (!make_map(&mp->s_store[b], bf, stage, vc, nc, vc * 2, 64, 32)) return false;
+    if (!make_map(&mp->s_k[b], bf, stage, vc, nc, vc * 2, 64, kBM)) return false;
+    if (!make_map(&mp->s_mn[b], bf, stage, vc, nc, vc * 2, 64, 64)) return false;
+  }
   if (!make_map(&mp->dh, f32, dH, D, N, D * 4, 32, 32)) return false;
   if (!make_map(&mp->dw, f32, dW, D, V, D * 4, 32, 32)) return false;
   return true;

@@ -89,6 +89,27 @@ struct GemmParams {
   uint64_t wait_limit_ns;
 };
 
+// One persistent launch runs up to kMaxProblems independent GEMM problems back
+// to back: tiles [0, tile_end[0]) belong to problem 0, [tile_end[0],
+// tile_end[1]) to problem 1, and so on. Problems in one launch must not read
+// what another writes.
+constexpr int kMaxProblems = 3;
+
+struct GemmLaunch {
+  CUtensorMap tm_a[kMaxProblems];
+  CUtensorMap tm_b[kMaxProblems];
+  CUtensorMap tm_out[kMaxProblems];
+  GemmParams prob[kMaxProblems];
+  int32_t n_probs;
+  int32_t tile_end[kMaxProblems];
+};
+
+__device__ __forceinline__ int decode_tile(const GemmLaunch& L, int t, int& pi) {
+  pi = 0;
+  while (pi < L.n_probs - 1 && t >= L.tile_end[pi]) ++pi;
+  return pi == 0 ? t : t - L.tile_end[pi - 1];
+}
+
 __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mt, int& nt) {
   if (p.n_fast) {
     nt = t % p.n_tiles;
@@ -116,14 +137,12 @@ __device__ __forceinline__ bool kblock_skipped(const GemmParams& p, int mt, int 
   return __ldg(p.flags + (size_t)srow * p.flags_ld + scol) == 0u;
 }
 
-__device__ __forceinline__ void record_timeout(const GemmParams& p, volatile uint32_t* abort_flag) {
+__device__ __forceinline__ void record_timeout(uint32_t* status, volatile uint32_t* abort_flag) {
   *abort_flag = 1u;
-  atomicOr(p.status, kDevTimeout);
+  atomicOr(status, kDevTimeout);
 }
 
-__global__ void __launch_bounds__(kGemmThreads, 1)
-    flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmOut, const GemmParams p) {
+__global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid_constant__ GemmLaunch L) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -139,7 +158,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_tiles = p.m_tiles * p.n_tiles;
+  const int num_tiles = L.tile_end[L.n_probs - 1];
+  const uint64_t wait_limit_ns = L.prob[0].wait_limit_ns;
+  uint32_t* const status = L.prob[0].status;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -153,9 +174,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0u;
     ptx::fence_mbarrier_init();
-    ptx::prefetch_tmap(&tmA);
-    ptx::prefetch_tmap(&tmB);
-    ptx::prefetch_tmap(&tmOut);
+    for (int q = 0; q < L.n_probs; ++q) {
+      ptx::prefetch_tmap(&L.tm_a[q]);
+      ptx::prefetch_tmap(&L.tm_b[q]);
+      ptx::prefetch_tmap(&L.tm_out[q]);
+    }
   }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, kTmemCols);
@@ -174,12 +197,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
       bool ok = true;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        int mt, nt;
-        tile_coords(p, t, mt, nt);
+        int pi, mt, nt;
+        const int tl = decode_tile(L, t, pi);
+        const GemmParams& p = L.prob[pi];
+        const CUtensorMap* tmA = &L.tm_a[pi];
+        const CUtensorMap* tmB = &L.tm_b[pi];
+        tile_coords(p, tl, mt, nt);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (kblock_skipped(p, mt, kb)) continue;
-          if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, p.wait_limit_ns, abort_flag)) {
-            record_timeout(p, abort_flag);
+          if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, wait_limit_ns, abort_flag)) {
+            record_timeout(status, abort_flag);
             ok = false;
             break;
           }
@@ -189,15 +216,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int32_t kc = kb * kBK;
           if (p.a_mn) {
             for (int h = 0; h < kBM / 64; ++h)
-              ptx::tma_load_2d(sa + h * 8192, &tmA, p.a_m0 + mt * kBM + h * 64, p.a_k0 + kc, &full_bar[stage]);
+              ptx::tma_load_2d(sa + h * 8192, tmA, p.a_m0 + mt * kBM + h * 64, p.a_k0 + kc, &full_bar[stage]);
           } else {
-            ptx::tma_load_2d(sa, &tmA, p.a_k0 + kc, p.a_m0 + mt * kBM, &full_bar[stage]);
+            ptx::tma_load_2d(sa, tmA, p.a_k0 + kc, p.a_m0 + mt * kBM, &full_bar[stage]);
           }
           if (p.b_mn) {
             for (int h = 0; h < kBN / 64; ++h)
-              ptx::tma_load_2d(sb + h * 8192, &tmB, p.b_n0 + nt * kBN + h * 64, p.b_k0 + kc, &full_bar[stage]);
+              ptx::tma_load_2d(sb + h * 8192, tmB, p.b_n0 + nt * kBN + h * 64, p.b_k0 + kc, &full_bar[stage]);
           } else {
-            ptx::tma_load_2d(sb, &tmB, p.b_k0 + kc, p.b_n0 + nt * kBN, &full_bar[stage]);
+            ptx::tma_load_2d(sb, tmB, p.b_k0 + kc, p.b_n0 + nt * kBN, &full_bar[stage]);
           }
           last_parity[stage] = (int32_t)phase;
           if (++stage == kStages) {
@@ -217,17 +244,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = ptx::idesc_bf16_f32(kBM, kBN, p.a_mn != 0, p.b_mn != 0);
       const uint32_t smem_base = ptx::smem_u32(smem);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       int i = 0;
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++i) {
-        int mt, nt;
-        tile_coords(p, t, mt, nt);
+        int pi, mt, nt;
+        const int tl = decode_tile(L, t, pi);
+        const GemmParams& p = L.prob[pi];
+        tile_coords(p, tl, mt, nt);
+        const uint32_t idesc = ptx::idesc_bf16_f32(kBM, kBN, p.a_mn != 0, p.b_mn != 0);
         const uint32_t buf = i & 1, use = i >> 1;
-        if (!ptx::mbar_wait_bounded(&acc_empty[buf], (use & 1u) ^ 1u, p.wait_limit_ns, abort_flag)) {
-          record_timeout(p, abort_flag);
+        if (!ptx::mbar_wait_bounded(&acc_empty[buf], (use & 1u) ^ 1u, wait_limit_ns, abort_flag)) {
+          record_timeout(status, abort_flag);
           ok = false;
           break;
         }
@@ -236,8 +265,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t accumulate = 0;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (kblock_skipped(p, mt, kb)) continue;
-          if (!ptx::mbar_wait_bounded(&full_bar[stage], phase, p.wait_limit_ns, abort_flag)) {
-            record_timeout(p, abort_flag);
+          if (!ptx::mbar_wait_bounded(&full_bar[stage], phase, wait_limit_ns, abort_flag)) {
+            record_timeout(status, abort_flag);
             ok = false;
             break;
           }
@@ -276,11 +305,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t ebuf = 0;
     int i = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++i) {
-      int mt, nt;
-      tile_coords(p, t, mt, nt);
+      int pi, mt, nt;
+      const int tl = decode_tile(L, t, pi);
+      const GemmParams& p = L.prob[pi];
+      const CUtensorMap* tmOut = &L.tm_out[pi];
+      tile_coords(p, tl, mt, nt);
       const uint32_t buf = i & 1, use = i >> 1;
-      if (!ptx::mbar_wait_bounded(&acc_full[buf], use & 1u, p.wait_limit_ns, abort_flag)) {
-        record_timeout(p, abort_flag);
+      if (!ptx::mbar_wait_bounded(&acc_full[buf], use & 1u, wait_limit_ns, abort_flag)) {
+        record_timeout(status, abort_flag);
         break;
       }
       ptx::tc_fence_after();
@@ -399,7 +431,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ptx::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            ptx::tma_store_2d(&tmOut, sbox, nt * kBN + box * 64, mt * kBM + q * 32);
+            ptx::tma_store_2d(tmOut, sbox, nt * kBN + box * 64, mt * kBM + q * 32);
             ptx::bulk_commit_group();
           }
           ebuf ^= 1u;
@@ -448,9 +480,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (lane == 0) {
               const int32_t c0 = nt * kBN + c, c1 = p.out_m0 + mt * kBM + q * 32;
               if (p.mode == EPI_REDUCE)
-                ptx::tma_reduce_add_2d(&tmOut, sbox, c0, c1);
+                ptx::tma_reduce_add_2d(tmOut, sbox, c0, c1);
               else
-                ptx::tma_store_2d(&tmOut, sbox, c0, c1);
+                ptx::tma_store_2d(tmOut, sbox, c0, c1);
               ptx::bulk_commit_group();
             }
             ebuf ^= 1u;

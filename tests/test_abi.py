@@ -37,7 +37,7 @@ def test_workspace_is_linear_in_rows_and_vocab_never_n_times_v():
     p = flce.make_problem(8192, 2048, 151552)
     ws = flce.flce_workspace_bytes(p)
     logits = 8192 * 151552 * 2
-    assert 0 < ws < logits / 10
+    assert 0 < ws < logits / 5
     # 16x the rows: O(N) growth only (row chunks reuse the same buffers).
     p_long = flce.make_problem(131072, 2048, 151552)
     ws_long = flce.flce_workspace_bytes(p_long)
