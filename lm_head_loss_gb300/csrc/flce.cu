@@ -22,6 +22,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -293,7 +294,10 @@ static bool device_setup(int* sms_out) {
   if (!info[dev].ready) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-    if (cudaFuncSetAttribute(flce_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(flce_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kGemmSmemBytes) != cudaSuccess)
+      return false;
+    if (cudaFuncSetAttribute(flce_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kGemmSmemBytes) != cudaSuccess)
       return false;
     info[dev].sms = sms;
@@ -303,34 +307,62 @@ static bool device_setup(int* sms_out) {
   return true;
 }
 
+// CTAs per cluster of the GEMM launches: 1 (independent CTAs) unless
+// FLCE_GEMM_CLUSTER=2 asks for pairs that share the B tile through TMA multicast.
+static int gemm_cluster() {
+  static int kc = [] {
+    const char* e = std::getenv("FLCE_GEMM_CLUSTER");
+    return (e && std::atoi(e) == 2) ? 2 : 1;
+  }();
+  return kc;
+}
+
 // Collects up to kMaxProblems GEMM problems for one persistent launch.
 struct Group {
   GemmLaunch L;
-  int tiles = 0;
-  Group() { std::memset(&L, 0, sizeof(L)); }
+  int units = 0;
+  int cluster;
+  explicit Group(int kc) : cluster(kc) { std::memset(&L, 0, sizeof(L)); }
   void add(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, const GemmParams& gp) {
-    const int t = gp.m_tiles * gp.n_tiles;
-    if (t <= 0) return;
+    const int u = (int)ceil_div(gp.m_tiles, cluster) * gp.n_tiles;
+    if (u <= 0) return;
     const int q = L.n_probs++;
     L.tm_a[q] = a;
     L.tm_b[q] = b;
     L.tm_out[q] = out;
     L.prob[q] = gp;
-    tiles += t;
-    L.tile_end[q] = tiles;
+    units += u;
+    L.tile_end[q] = units;
   }
 };
 
 static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
-  if (g.tiles <= 0) return true;
-  const int grid = std::min(g.tiles, sms);
+  if (g.units <= 0) return true;
   ProfScope prof(kind, st);
-  flce_gemm_kernel<<<grid, kGemmThreads, kGemmSmemBytes, st>>>(g.L);
-  return cudaGetLastError() == cudaSuccess;
+  if (g.cluster == 1) {
+    const int grid = std::min(g.units, sms);
+    flce_gemm_kernel<1><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(g.L);
+    return cudaGetLastError() == cudaSuccess;
+  }
+  const int grid = 2 * std::min(g.units, sms / 2);
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
+  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, flce_gemm_kernel<2>, g.L) == cudaSuccess;
 }
 
 struct Maps {
-  CUtensorMap h_k, w_k, h_mn, w_mn, dh, dw;
+  CUtensorMap h_k, w_k, w_k_half, h_mn, w_mn, dh, dw;
   CUtensorMap s_store[2], s_k[2], s_mn[2];   // one set per staging buffer
 };
 
@@ -378,8 +410,9 @@ static flce_status run_forward(const flce_problem& p, const Plan& pl, const Maps
     gp.part_m = part_m;
     gp.part_s = part_s;
     gp.zy = zy;
-    Group g;
-    g.add(mp.h_k, mp.w_k, mp.h_k, gp);
+    const int kc = gemm_cluster();
+    Group g(kc);
+    g.add(mp.h_k, kc == 1 ? mp.w_k : mp.w_k_half, mp.h_k, gp);
     if (!launch_group(FLCE_KERNEL_GEMM_LSE, g, sms, st)) return FLCE_ERR_CUDA;
     ProfScope prof(FLCE_KERNEL_COMBINE, st);
     lse_combine_kernel<<<(int)ceil_div(rows, kCombineThreads), kCombineThreads, 0, st>>>(
@@ -439,10 +472,12 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     return cudaGetLastError() == cudaSuccess;
   };
 
+  const int kc = gemm_cluster();
+  const CUtensorMap& w_b = kc == 1 ? mp.w_k : mp.w_k_half;
   {
-    Group g;
+    Group g(kc);
     const GemmParams dz0 = dz_params(0);
-    g.add(mp.h_k, mp.w_k, mp.s_store[0], dz0);
+    g.add(mp.h_k, w_b, mp.s_store[0], dz0);
     if (!launch_group(FLCE_KERNEL_GEMM_DZ, g, sms, st)) return FLCE_ERR_CUDA;
     if (!count_skipped(dz0)) return FLCE_ERR_CUDA;
   }
@@ -453,7 +488,7 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     item_geom(s, r0, rows, v0, cols);
     const int rc = s / pl.v_chunks, vi = s % pl.v_chunks;
     uint32_t* flags = reinterpret_cast<uint32_t*>(ws + pl.off_flags[b]);
-    Group g;
+    Group g(kc);
     // dW[v0 : v0+cols, :] (=|+=) scale * staging^T * H[r0 : r0+rows, :]
     GemmParams dw = base_params(p, hdr);
     dw.m_tiles = (int)ceil_div(cols, kBM);
@@ -466,7 +501,7 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     dw.mode = rc == 0 ? EPI_STORE : EPI_REDUCE;
     dw.out_m0 = (int32_t)v0;
     dw.scale = &hdr->scale;
-    dw.filter = filter;
+    dw.skip_by_flags = filter;
     dw.flags = flags;
     dw.flags_ld = pl.vc / kBN;
     dw.flags_a_is_rows = 0;
@@ -483,7 +518,7 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     dh.mode = vi == 0 ? EPI_STORE : EPI_REDUCE;
     dh.out_m0 = (int32_t)r0;
     dh.scale = &hdr->scale;
-    dh.filter = filter;
+    dh.skip_by_flags = filter;
     dh.flags = flags;
     dh.flags_ld = pl.vc / kBN;
     dh.flags_a_is_rows = 1;
@@ -492,7 +527,7 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     const bool has_next = s + 1 < items;
     if (has_next) {
       dz_next = dz_params(s + 1);
-      g.add(mp.h_k, mp.w_k, mp.s_store[b ^ 1], dz_next);
+      g.add(mp.h_k, w_b, mp.s_store[b ^ 1], dz_next);
     }
     if (!launch_group(FLCE_KERNEL_GEMM_BWD, g, sms, st)) return FLCE_ERR_CUDA;
     if (has_next && !count_skipped(dz_next)) return FLCE_ERR_CUDA;
@@ -506,6 +541,7 @@ static bool build_maps(const flce_problem& p, const Plan& pl, const void* H, con
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   if (!make_map(&mp->h_k, bf, H, D, N, D * 2, 64, kBM)) return false;
   if (!make_map(&mp->w_k, bf, W, D, V, D * 2, 64, kBN)) return false;
+  if (!make_map(&mp->w_k_half, bf, W, D, V, D * 2, 64, kBN / 2)) return false;
   if (!backward) return true;
   if (!make_map(&mp->h_mn, bf, H, D, N, D * 2, 64, 64)) return false;
   if (!make_map(&mp->w_mn, bf, W, D, V, D * 2, 64, 64)) return false;

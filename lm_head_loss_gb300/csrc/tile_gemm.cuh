@@ -73,7 +73,8 @@ struct GemmParams {
   int32_t out_m0;              // STORE / REDUCE: row coordinate offset in the output map
   int32_t part_ld;             // LSE: leading dimension of the partial arrays
   int32_t part_t0;             // LSE: partial index of n-tile 0
-  int32_t filter;              // DZ: write skip flags; STORE/REDUCE: honour them
+  int32_t filter;              // DZ: write the per-tile skip flags
+  int32_t skip_by_flags;       // STORE/REDUCE: leave out k-blocks whose dZ tiles were filtered
   float filter_eps;
   int64_t ignore_index;
   const int64_t* y;
@@ -104,20 +105,27 @@ struct GemmLaunch {
   int32_t tile_end[kMaxProblems];
 };
 
+// Tiles are counted in groups of kCluster vertically adjacent m-tiles that
+// share one n-tile (one group per cluster); with kCluster = 1 a group is a tile.
+__device__ __forceinline__ int m_groups(const GemmParams& p, int cluster) { return (p.m_tiles + cluster - 1) / cluster; }
+
 __device__ __forceinline__ int decode_tile(const GemmLaunch& L, int t, int& pi) {
   pi = 0;
   while (pi < L.n_probs - 1 && t >= L.tile_end[pi]) ++pi;
   return pi == 0 ? t : t - L.tile_end[pi - 1];
 }
 
-__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mt, int& nt) {
+__device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int cluster, int rank, int& mt, int& nt) {
+  int mg;
   if (p.n_fast) {
     nt = t % p.n_tiles;
-    mt = t / p.n_tiles;
+    mg = t / p.n_tiles;
   } else {
-    mt = t % p.m_tiles;
-    nt = t / p.m_tiles;
+    const int groups = m_groups(p, cluster);
+    mg = t % groups;
+    nt = t / groups;
   }
+  mt = mg * cluster + rank;
 }
 
 // Whether k-block kb of tile (mt, nt) reads only dZ tiles whose gradient was
@@ -125,7 +133,8 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int& mt,
 //   dH (flags_a_is_rows = 1): A = staging rows mt*128.., columns kb*64..
 //   dW (flags_a_is_rows = 0): A = staging^T, rows kb*64.., columns mt*128..
 __device__ __forceinline__ bool kblock_skipped(const GemmParams& p, int mt, int kb) {
-  if (!p.filter) return false;
+  if (!p.skip_by_flags) return false;
+  if (mt >= p.m_tiles) return true;            // the empty half of a cluster's last group
   int srow, scol;
   if (p.flags_a_is_rows) {
     srow = mt;
@@ -137,11 +146,26 @@ __device__ __forceinline__ bool kblock_skipped(const GemmParams& p, int mt, int 
   return __ldg(p.flags + (size_t)srow * p.flags_ld + scol) == 0u;
 }
 
+// A k-block is left out by the whole cluster only when every CTA of it skips it.
+template <int kCluster>
+__device__ __forceinline__ bool kblock_skipped_group(const GemmParams& p, int mt_first, int kb) {
+  bool all = true;
+#pragma unroll
+  for (int r = 0; r < kCluster; ++r) all = all && kblock_skipped(p, mt_first + r, kb);
+  return all;
+}
+
 __device__ __forceinline__ void record_timeout(uint32_t* status, volatile uint32_t* abort_flag) {
   *abort_flag = 1u;
   atomicOr(status, kDevTimeout);
 }
 
+// kCluster = 1: every CTA loads its own A and B tiles.
+// kCluster = 2: the two CTAs of a cluster take vertically adjacent m-tiles of
+// the same n-tile; each loads its own A tile and one half of the shared B tile
+// and multicasts that half into both CTAs, so the cluster reads B from L2 once.
+// A shared-memory stage is refilled only after both CTAs' MMAs have read it.
+template <int kCluster>
 __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid_constant__ GemmLaunch L) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -159,13 +183,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_tiles = L.tile_end[L.n_probs - 1];
+  const int rank = kCluster > 1 ? (int)ptx::cluster_ctarank() : 0;
+  const int unit0 = blockIdx.x / kCluster;
+  const int unit_stride = gridDim.x / kCluster;
+  constexpr uint16_t kPeers = (uint16_t)((1u << kCluster) - 1u);
   const uint64_t wait_limit_ns = L.prob[0].wait_limit_ns;
   uint32_t* const status = L.prob[0].status;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
-      ptx::mbar_init(&empty_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], kCluster);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&acc_full[b], 1);
@@ -186,6 +214,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
   }
   ptx::tc_fence_before();
   __syncthreads();
+  if (kCluster > 1) ptx::cluster_sync_all();   // peers' barriers exist before any multicast
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -196,15 +225,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
       int32_t last_parity[kStages];
       for (int s = 0; s < kStages; ++s) last_parity[s] = -1;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      for (int t = unit0; t < num_tiles && ok; t += unit_stride) {
         int pi, mt, nt;
         const int tl = decode_tile(L, t, pi);
         const GemmParams& p = L.prob[pi];
         const CUtensorMap* tmA = &L.tm_a[pi];
         const CUtensorMap* tmB = &L.tm_b[pi];
-        tile_coords(p, tl, mt, nt);
+        tile_coords(p, tl, kCluster, rank, mt, nt);
+        const int mt_first = mt - rank;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (kblock_skipped(p, mt, kb)) continue;
+          if (kblock_skipped_group<kCluster>(p, mt_first, kb)) continue;
           if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
@@ -220,11 +250,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
           } else {
             ptx::tma_load_2d(sa, tmA, p.a_k0 + kc, p.a_m0 + mt * kBM, &full_bar[stage]);
           }
-          if (p.b_mn) {
-            for (int h = 0; h < kBN / 64; ++h)
-              ptx::tma_load_2d(sb + h * 8192, tmB, p.b_n0 + nt * kBN + h * 64, p.b_k0 + kc, &full_bar[stage]);
+          if (kCluster == 1) {
+            if (p.b_mn) {
+              for (int h = 0; h < kBN / 64; ++h)
+                ptx::tma_load_2d(sb + h * 8192, tmB, p.b_n0 + nt * kBN + h * 64, p.b_k0 + kc, &full_bar[stage]);
+            } else {
+              ptx::tma_load_2d(sb, tmB, p.b_k0 + kc, p.b_n0 + nt * kBN, &full_bar[stage]);
+            }
           } else {
-            ptx::tma_load_2d(sb, tmB, p.b_k0 + kc, p.b_n0 + nt * kBN, &full_bar[stage]);
+            // This CTA's share of the B tile: rows [rank * kBN / kCluster, ...).
+            constexpr int kShare = kBN / kCluster;
+            if (p.b_mn) {
+              for (int h = rank * (kShare / 64); h < (rank + 1) * (kShare / 64); ++h)
+                ptx::tma_load_2d_multicast(sb + h * 8192, tmB, p.b_n0 + nt * kBN + h * 64, p.b_k0 + kc,
+                                           &full_bar[stage], kPeers);
+            } else {
+              ptx::tma_load_2d_multicast(sb + rank * kShare * 128, tmB, p.b_k0 + kc, p.b_n0 + nt * kBN + rank * kShare,
+                                         &full_bar[stage], kPeers);
+            }
           }
           last_parity[stage] = (int32_t)phase;
           if (++stage == kStages) {
@@ -248,11 +291,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       int i = 0;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++i) {
+      for (int t = unit0; t < num_tiles && ok; t += unit_stride, ++i) {
         int pi, mt, nt;
         const int tl = decode_tile(L, t, pi);
         const GemmParams& p = L.prob[pi];
-        tile_coords(p, tl, mt, nt);
+        tile_coords(p, tl, kCluster, rank, mt, nt);
+        const int mt_first = mt - rank;
         const uint32_t idesc = ptx::idesc_bf16_f32(kBM, kBN, p.a_mn != 0, p.b_mn != 0);
         const uint32_t buf = i & 1, use = i >> 1;
         if (!ptx::mbar_wait_bounded(&acc_empty[buf], (use & 1u) ^ 1u, wait_limit_ns, abort_flag)) {
@@ -264,25 +308,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
         const uint32_t d_tmem = tmem_base + buf * kBN;
         uint32_t accumulate = 0;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (kblock_skipped(p, mt, kb)) continue;
+          if (kblock_skipped_group<kCluster>(p, mt_first, kb)) continue;
           if (!ptx::mbar_wait_bounded(&full_bar[stage], phase, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t a_addr = smem_base + stage * kStageBytes;
-          const uint32_t b_addr = a_addr + kABytes;
+          // In a cluster, a stage the group loads for the peer may still be
+          // one this CTA's own tile skips: it then issues no MMA but still
+          // releases the stage.
+          if (kCluster == 1 || !kblock_skipped(p, mt, kb)) {
+            const uint32_t a_addr = smem_base + stage * kStageBytes;
+            const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t adesc = p.a_mn ? ptx::smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
-                                          : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
-            const uint64_t bdesc = p.b_mn ? ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
-                                          : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
-            ptx::mma_bf16_ss(d_tmem, adesc, bdesc, idesc, accumulate);
-            accumulate = 1;
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint64_t adesc = p.a_mn ? ptx::smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                            : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
+              const uint64_t bdesc = p.b_mn ? ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                            : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
+              ptx::mma_bf16_ss(d_tmem, adesc, bdesc, idesc, accumulate);
+              accumulate = 1;
+            }
           }
-          ptx::mma_commit(&empty_bar[stage]);
+          if (kCluster == 1)
+            ptx::mma_commit(&empty_bar[stage]);
+          else
+            ptx::mma_commit_multicast(&empty_bar[stage], kPeers);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -304,12 +356,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
     uint8_t* my_boxes = epi_smem + q * 2 * kEpiBoxBytes;
     uint32_t ebuf = 0;
     int i = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++i) {
+    for (int t = unit0; t < num_tiles; t += unit_stride, ++i) {
       int pi, mt, nt;
       const int tl = decode_tile(L, t, pi);
       const GemmParams& p = L.prob[pi];
       const CUtensorMap* tmOut = &L.tm_out[pi];
-      tile_coords(p, tl, mt, nt);
+      tile_coords(p, tl, kCluster, rank, mt, nt);
       const uint32_t buf = i & 1, use = i >> 1;
       if (!ptx::mbar_wait_bounded(&acc_full[buf], use & 1u, wait_limit_ns, abort_flag)) {
         record_timeout(status, abort_flag);
@@ -319,7 +371,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
       const uint32_t taddr = tmem_base + buf * kBN + ((uint32_t)(q * 32) << 16);
       const int lrow = mt * kBM + r_local;     // local row of this launch
 
-      if (p.mode == EPI_LSE) {
+      if (mt >= p.m_tiles) {
+        // The empty half of a cluster's last group: nothing to write.
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
+      } else if (p.mode == EPI_LSE) {
         const bool in_rows = lrow < p.m_valid && (p.row0 + lrow) < p.n_rows;
         const int grow = p.row0 + lrow;
         const int col_t0 = p.col0 + nt * kBN;
@@ -447,8 +504,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
         }
       } else {
         // EPI_STORE / EPI_REDUCE
-        bool all_skipped = p.filter != 0;
-        if (p.filter) {
+        bool all_skipped = p.skip_by_flags != 0;
+        if (p.skip_by_flags) {
           for (int kb = 0; kb < p.k_blocks && all_skipped; ++kb) all_skipped = kblock_skipped(p, mt, kb);
         }
         const float sc = __ldg(p.scale);
@@ -499,6 +556,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
 
   ptx::tc_fence_before();
   __syncthreads();
+  if (kCluster > 1) ptx::cluster_sync_all();   // no peer still multicasts into this CTA
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
 }
