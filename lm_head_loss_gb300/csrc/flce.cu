@@ -33,7 +33,6 @@ namespace flce {
 
 constexpr int kRowChunk = 8192;    // rows per chunk (multiple of 256)
 constexpr int kVocabChunk = 8192;  // vocabulary ids per backward chunk (multiple of 256)
-constexpr int kCombineThreads = 256;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kShortWaitNs = 1000ull;
 
@@ -90,40 +89,57 @@ __global__ void prep_kernel(const int64_t* __restrict__ y, int64_t n, int64_t vo
   }
 }
 
-// One thread per row of a row chunk: merge the per-tile (max, sum) partials
-// in tile order into LSE_n, then sum the row losses of the block in a fixed
-// tree order (fp64).
-__global__ void lse_combine_kernel(const float* __restrict__ part_m, const float* __restrict__ part_s, int part_ld,
-                                   int n_tiles, const float* __restrict__ zy, const int64_t* __restrict__ y,
-                                   int64_t row0, int rows, int64_t vocab, int64_t ignore_index,
-                                   float* __restrict__ lse_out, double* __restrict__ block_sums) {
-  __shared__ double red[kCombineThreads];
-  const int lr = blockIdx.x * kCombineThreads + threadIdx.x;
-  double contrib = 0.0;
+// Merge of the per-tile (max, sum) partials into LSE_n. A block covers 32
+// rows; thread (r, g) merges tiles g, g + 8, g + 16, ... of row r, then the 8
+// partials of a row are merged in g order and the 32 row losses of the block
+// are summed in a fixed tree order (fp64).
+constexpr int kCombineRows = 32;
+constexpr int kCombineSplit = 8;
+
+__device__ __forceinline__ void lse_merge(float& mx, float& sm, float m, float s) {
+  if (m > mx) {
+    sm = sm * exp2f(mx - m) + s;
+    mx = m;
+  } else {
+    sm += s * exp2f(m - mx);
+  }
+}
+
+__global__ void __launch_bounds__(kCombineRows * kCombineSplit)
+    lse_combine_kernel(const float* __restrict__ part_m, const float* __restrict__ part_s, int part_ld, int n_tiles,
+                       const float* __restrict__ zy, const int64_t* __restrict__ y, int64_t row0, int rows,
+                       int64_t vocab, int64_t ignore_index, float* __restrict__ lse_out,
+                       double* __restrict__ block_sums) {
+  __shared__ float sh_m[kCombineSplit][kCombineRows];
+  __shared__ float sh_s[kCombineSplit][kCombineRows];
+  __shared__ double red[kCombineRows];
+  const int r = threadIdx.x, g = threadIdx.y;
+  const int lr = blockIdx.x * kCombineRows + r;
+  float mx = -INFINITY, sm = 0.f;
   if (lr < rows) {
-    float mx = -INFINITY, sm = 0.f;
-    for (int t = 0; t < n_tiles; ++t) {
-      const float m = part_m[(size_t)t * part_ld + lr];
-      const float s = part_s[(size_t)t * part_ld + lr];
-      if (m > mx) {
-        sm = sm * exp2f(mx - m) + s;
-        mx = m;
-      } else {
-        sm += s * exp2f(m - mx);
-      }
-    }
-    const float lse = (mx + log2f(sm)) * 0.69314718055994531f;
-    lse_out[row0 + lr] = lse;
-    const int64_t t = y[row0 + lr];
-    if (t != ignore_index && t >= 0 && t < vocab) contrib = (double)lse - (double)zy[lr];
+    for (int t = g; t < n_tiles; t += kCombineSplit)
+      lse_merge(mx, sm, part_m[(size_t)t * part_ld + lr], part_s[(size_t)t * part_ld + lr]);
   }
-  red[threadIdx.x] = contrib;
+  sh_m[g][r] = mx;
+  sh_s[g][r] = sm;
   __syncthreads();
-  for (int s = kCombineThreads / 2; s > 0; s >>= 1) {
-    if (threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
-    __syncthreads();
+  if (g == 0) {
+    double contrib = 0.0;
+    if (lr < rows) {
+      for (int k = 1; k < kCombineSplit; ++k) lse_merge(mx, sm, sh_m[k][r], sh_s[k][r]);
+      const float lse = (mx + log2f(sm)) * 0.69314718055994531f;
+      lse_out[row0 + lr] = lse;
+      const int64_t t = y[row0 + lr];
+      if (t != ignore_index && t >= 0 && t < vocab) contrib = (double)lse - (double)zy[lr];
+    }
+    red[r] = contrib;
   }
-  if (threadIdx.x == 0) block_sums[row0 / kCombineThreads + blockIdx.x] = red[0];
+  __syncthreads();
+  if (g == 0 && r == 0) {
+    double acc = 0.0;
+    for (int k = 0; k < kCombineRows; ++k) acc += red[k];
+    block_sums[row0 / kCombineRows + blockIdx.x] = acc;
+  }
 }
 
 // One block: fixed-order fp64 sum of the per-block row losses, mean over the
@@ -207,12 +223,13 @@ struct Plan {
   size_t off_pm, off_ps, off_zy, off_lse, off_bsum, off_flags[2], off_stage[2], total;
 };
 
-static Plan make_plan(const flce_problem& p) {
+// Workspace layout for a row chunk of nc rows (a multiple of 256).
+static Plan make_plan_rows(const flce_problem& p, int nc) {
   Plan pl{};
   pl.n = p.n_rows;
   pl.d = p.hidden;
   pl.v = p.vocab;
-  pl.nc = (int)std::min<int64_t>(align_up((size_t)std::max<int64_t>(p.n_rows, 1), 256), kRowChunk);
+  pl.nc = nc;
   pl.vc = (int)std::min<int64_t>(align_up((size_t)p.vocab, 256), kVocabChunk);
   pl.n_vtiles = (int)ceil_div(p.vocab, kBN);
   pl.row_chunks = (int)ceil_div(std::max<int64_t>(p.n_rows, 1), pl.nc);
@@ -227,7 +244,7 @@ static Plan make_plan(const flce_problem& p) {
   pl.off_lse = off;
   off = align_up(off + (size_t)std::max<int64_t>(p.n_rows, 1) * 4, 1024);
   pl.off_bsum = off;
-  off = align_up(off + (size_t)pl.row_chunks * (pl.nc / kCombineThreads) * 8, 1024);
+  off = align_up(off + (size_t)pl.row_chunks * (pl.nc / kCombineRows) * 8, 1024);
   for (int b = 0; b < 2; ++b) {
     pl.off_flags[b] = off;
     off = align_up(off + (size_t)(pl.nc / kBM) * (pl.vc / kBN) * 4, 1024);
@@ -238,6 +255,10 @@ static Plan make_plan(const flce_problem& p) {
   }
   pl.total = off;
   return pl;
+}
+
+static Plan make_plan(const flce_problem& p) {
+  return make_plan_rows(p, (int)std::min<int64_t>(align_up((size_t)std::max<int64_t>(p.n_rows, 1), 256), kRowChunk));
 }
 
 static bool problem_ok(const flce_problem* p) {
@@ -415,11 +436,11 @@ static flce_status run_forward(const flce_problem& p, const Plan& pl, const Maps
     g.add(mp.h_k, kc == 1 ? mp.w_k : mp.w_k_half, mp.h_k, gp);
     if (!launch_group(FLCE_KERNEL_GEMM_LSE, g, sms, st)) return FLCE_ERR_CUDA;
     ProfScope prof(FLCE_KERNEL_COMBINE, st);
-    lse_combine_kernel<<<(int)ceil_div(rows, kCombineThreads), kCombineThreads, 0, st>>>(
+    lse_combine_kernel<<<(int)ceil_div(rows, kCombineRows), dim3(kCombineRows, kCombineSplit), 0, st>>>(
         part_m, part_s, pl.nc, pl.n_vtiles, zy, y, r0, rows, p.vocab, p.ignore_index, lse, bsum);
     if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
   }
-  const int n_blocks = (int)ceil_div(p.n_rows, kCombineThreads);
+  const int n_blocks = (int)ceil_div(p.n_rows, kCombineRows);
   ProfScope prof(FLCE_KERNEL_FINALIZE, st);
   finalize_kernel<<<1, 256, 0, st>>>(bsum, n_blocks, grad_loss, hdr, loss);
   if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;

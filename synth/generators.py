@@ -219,6 +219,9 @@ WORKLOADS: dict[str, Workload] = {
                                 description="Gravity-16B-A3B-shaped head, B=1 S=8192"),
     "gemma2_2b_head": Workload("gemma2_2b_head", 8192, 2304, 256000, 9.0, "top16", 0.0,
                                description="Gemma-2-2B-shaped head, peaky softmax"),
+    "gravity16b_head_v65536": Workload("gravity16b_head_v65536", 8192, 2048, 65536, 1.0, "zipf", 0.02,
+                                       description="Gravity-16B-A3B head with the vocabulary cut to 65536, "
+                                                   "for profiler captures (about 1.3 GB on the device)"),
     "long128k_head": Workload("long128k_head", 131072, 2048, 151552, 1.0, "zipf", 0.10,
                               description="Gravity-16B-A3B head at 128K context"),
 }

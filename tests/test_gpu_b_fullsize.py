@@ -72,7 +72,13 @@ def _check_sampled(inp, got, full_forward: bool, seed=0):
     report["dH_rel_sampled"] = float(np.max(np.abs(got["dH"][rows] - dH_ref)) / np.max(np.abs(dH_ref)))
     dW64 = got["dW"].astype(np.float64)
     dH64 = got["dH"].astype(np.float64)
-    report["dW_colsum_rel"] = float(np.max(np.abs(dW64.sum(axis=0))) / np.max(np.abs(dW64)))
+    # sum_v dW_v = (g/count) sum_n (sum_v G_nv) H_n vanishes for exact G. The
+    # GPU rounds G to bf16 (relative error <= 2^-9 per element) and
+    # sum_v |G_nv| <= 2, so |sum_v dW_v[d]| <= 2^-8 (g/count) sum_n |H_nd|;
+    # the check reports the column sums against that bound (<= 1 passes).
+    valid = y != -100
+    bound = 2.0 ** -8 / max(valid.sum(), 1) * np.abs(H64[valid]).sum(axis=0)
+    report["dW_colsum_over_bf16_bound"] = float(np.max(np.abs(dW64.sum(axis=0)) / bound))
     a, b = float(np.sum(W64 * dW64)), float(np.sum(H64 * dH64))
     report["inner_product_rel"] = abs(a - b) / max(abs(a), abs(b))
     return report
@@ -80,7 +86,9 @@ def _check_sampled(inp, got, full_forward: bool, seed=0):
 
 def _assert_report(r):
     for k, v in r.items():
-        if k.startswith("lse_abs"):
+        if k == "dW_colsum_over_bf16_bound":
+            assert v <= 1.0, r
+        elif k.startswith("lse_abs"):
             assert v <= LSE_ABS, r
         elif k.startswith("loss_rel"):
             assert v <= LOSS_REL, r
