@@ -120,6 +120,30 @@ const char* flce_status_string(flce_status s);
  * Synchronises `stream`. Returns 0 when filtering was off. */
 flce_status flce_get_filter_stats(void* ws, void* stream, double* skipped_fraction);
 
+/* flce_forward without a caller-provided workspace, for callers that cannot
+ * allocate device memory at the point they need the loss: for example a
+ * plugin of an inference or training engine whose execute step must not
+ * allocate, or code that runs under a fixed memory budget set at start-up
+ * and has no spare buffer to hand over. The paper has no counterpart of this
+ * entry point; it exists for such callers.
+ *   Same arguments and results as flce_forward, minus ws and ws_bytes.
+ *   The scratch it uses is a 16 MiB array in device memory that the library
+ *   declares statically: every GPU that loads the library holds it until the
+ *   process exits. The call allocates and frees nothing.
+ *   Rows are processed in chunks small enough for the scratch. A problem
+ *   whose buffers do not fit even with 256-row chunks (roughly V above two
+ *   million) returns FLCE_ERR_UNSUPPORTED before launching anything.
+ *   The first call on a device looks up the scratch's device address (a
+ *   runtime API call); make that first call before any stream capture.
+ *   All calls share the one array and it keeps the last call's contents; the
+ *   call initialises everything it reads. Calls that overlap on the GPU (on
+ *   different streams, or from different threads) race on the scratch and
+ *   must be serialised by the caller.
+ *   Device-detected conditions (a bad target) are handled as in
+ *   flce_forward, but are not reported: there is no workspace to query. */
+flce_status flce_forward_static_scratch(const flce_problem* p, const void* H, const void* W, const int64_t* y,
+                                        float* lse, float* loss, void* stream);
+
 /* Launch timing for profiling. After flce_profile_set(events, kinds, cap),
  * every kernel the compute calls enqueue is bracketed by two CUDA events
  * taken from `events` (cudaEvent_t handles created by the caller with timing

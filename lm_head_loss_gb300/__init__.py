@@ -14,6 +14,7 @@ from ._binding import (  # noqa: F401
     declared_symbols,
     flce_forward,
     flce_forward_backward,
+    flce_forward_static_scratch,
     flce_get_device_status,
     flce_get_filter_stats,
     flce_status_string,

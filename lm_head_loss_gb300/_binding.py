@@ -72,6 +72,8 @@ def _load() -> ctypes.CDLL:
     lib.flce_status_string.restype = ctypes.c_char_p
     lib.flce_get_filter_stats.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_double)]
     lib.flce_get_filter_stats.restype = ctypes.c_int
+    lib.flce_forward_static_scratch.argtypes = [prob, vp, vp, vp, vp, vp, vp]
+    lib.flce_forward_static_scratch.restype = ctypes.c_int
     lib.flce_profile_set.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]
     lib.flce_profile_set.restype = ctypes.c_int
     lib.flce_profile_count.argtypes = []
@@ -126,6 +128,14 @@ def flce_forward_backward(problem, H, W, y, grad_loss: float, lse, loss, dH, dW,
     return Status(lib.flce_forward_backward(ctypes.byref(problem) if problem is not None else None, _addr(H),
                                             _addr(W), _addr(y), float(grad_loss), _addr(lse), _addr(loss),
                                             _addr(dH), _addr(dW), _addr(ws), nb, _stream(stream)))
+
+
+def flce_forward_static_scratch(problem, H, W, y, lse, loss, stream=None) -> Status:
+    """flce_forward for callers that cannot hand over a workspace (no device
+    allocation at call time); its scratch is a fixed 16 MiB array inside the
+    library."""
+    return Status(lib.flce_forward_static_scratch(ctypes.byref(problem) if problem is not None else None, _addr(H),
+                                                  _addr(W), _addr(y), _addr(lse), _addr(loss), _stream(stream)))
 
 
 def flce_get_device_status(ws, stream=None) -> Status:

@@ -592,6 +592,39 @@ static flce_status check_common(const flce_problem* p, const void* H, const void
   return FLCE_OK;
 }
 
+// ------------------------------------------------------------------ static scratch
+// Workspace of flce_forward_static_scratch: a fixed array in device memory
+// that every GPU loading this library holds until the process exits. Host
+// code must not pass the symbol itself to a kernel (on the host it names a
+// stand-in object, not device memory); the device address comes from
+// cudaGetSymbolAddress, looked up once per device.
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+static bool static_scratch_address(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_static_scratch) != cudaSuccess || !a) return false;
+    addr[dev] = a;
+  }
+  *out = addr[dev];
+  return true;
+}
+
+// Largest row chunk (a multiple of 256, at most the usual one) whose forward
+// buffers fit in the static scratch; 0 when even 256 rows do not fit.
+static int static_scratch_row_chunk(const flce_problem& p) {
+  int nc = (int)std::min<int64_t>(align_up((size_t)std::max<int64_t>(p.n_rows, 1), 256), kRowChunk);
+  for (; nc >= 256; nc -= 256)
+    if (make_plan_rows(p, nc).off_flags[0] <= kStaticScratchBytes) return nc;
+  return 0;
+}
+
 }  // namespace flce
 
 using namespace flce;
@@ -680,6 +713,25 @@ flce_status flce_get_filter_stats(void* ws, void* stream, double* skipped_fracti
   if (cudaMemcpy(&h, ws, sizeof(WsHeader), cudaMemcpyDeviceToHost) != cudaSuccess) return FLCE_ERR_CUDA;
   *skipped_fraction = (h.filter_on && h.tiles_total) ? (double)h.tiles_skipped / (double)h.tiles_total : 0.0;
   return FLCE_OK;
+}
+
+flce_status flce_forward_static_scratch(const flce_problem* p, const void* H, const void* W, const int64_t* y,
+                                        float* lse, float* loss, void* stream) {
+  if (!problem_ok(p) || !loss || !W || (p->n_rows > 0 && (!H || !y || !lse))) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(y, 8)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->hidden % 8 != 0 || !aligned(H, 16) || !aligned(W, 16)) return FLCE_ERR_UNSUPPORTED;
+  const int nc = static_scratch_row_chunk(*p);
+  if (nc == 0) return FLCE_ERR_UNSUPPORTED;   // the problem's buffers exceed the static scratch
+  int sms = 0;
+  if (!device_setup(&sms)) return FLCE_ERR_CUDA;
+  void* scratch = nullptr;
+  if (!static_scratch_address(&scratch)) return FLCE_ERR_CUDA;
+  const Plan pl = make_plan_rows(*p, nc);
+  Maps mp;
+  if (p->n_rows > 0 && !build_maps(*p, pl, H, W, nullptr, nullptr, static_cast<uint8_t*>(scratch), false, &mp))
+    return FLCE_ERR_CUDA;
+  return run_forward(*p, pl, mp, y, lse, loss, 1.0f, static_cast<uint8_t*>(scratch), sms,
+                     static_cast<cudaStream_t>(stream));
 }
 
 flce_status flce_profile_set(void** events, int32_t* kinds, int32_t cap) {

@@ -19,7 +19,7 @@ def test_library_exports_every_declared_symbol():
     declared = flce.declared_symbols()
     assert set(declared) == {"flce_workspace_bytes", "flce_forward", "flce_forward_backward",
                              "flce_get_device_status", "flce_status_string", "flce_get_filter_stats",
-                             "flce_profile_set", "flce_profile_count"}
+                             "flce_profile_set", "flce_profile_count", "flce_forward_static_scratch"}
     out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
     for name in declared:
