@@ -12,6 +12,7 @@ from .flce_oracle import (  # noqa: F401
     dW_rows,
     forward,
     forward_backward,
+    forward_backward_ex,
     forward_backward_filtered,
     inputs_f64,
     logits,

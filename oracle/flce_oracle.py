@@ -210,3 +210,58 @@ def forward_backward_filtered(H, W, y, eps: float, tile_rows: int, tile_cols: in
         dH[r0:r1] = dz @ W
         dW += dz.T @ H[r0:r1]
     return lse, loss, dH, dW, count, skipped / max(tiles, 1)
+
+
+def forward_backward_ex(H, W, y, bias=None, reduction: str = "mean", grad=1.0,
+                        ignore_index: int = IGNORE_INDEX, need_grad: bool = True):
+    """The general form: optional bias, reduction mean | sum | none.
+
+    With a bias b [V] the logits are z_n = H_n W^T + b (the PyTorch 2.13
+    chapter's linear_bias argument of F.linear_cross_entropy). Per-row losses
+    l_n = LSE_n - z_{n,y_n} (0 on ignored rows) are reduced to
+      mean: sum_n l_n / max(count, 1),  sum: sum_n l_n,  none: the vector l.
+    `grad` is the upstream gradient of the result: a scalar for mean/sum, a
+    length-N vector for none. dZ_nv = s_n * valid_n * (exp(z_nv - LSE_n) - [v = y_n])
+    with s_n = grad/max(count,1), grad, or grad[n]; dH = dZ W, dW = dZ^T H,
+    db = sum_n dZ_n. Returns a dict with lse, loss, count and, if need_grad,
+    dH, dW, db (db is None without a bias).
+    """
+    n, vocab = H.shape[0], W.shape[0]
+    y = _check_targets(y, vocab, ignore_index)
+    if reduction not in ("mean", "sum", "none"):
+        raise ValueError(reduction)
+    count = valid_count(y, ignore_index)
+    valid = y != ignore_index
+    if reduction == "none":
+        g = np.broadcast_to(np.asarray(grad, dtype=np.float64), (n,))
+        row_scale = g
+    else:
+        g0 = float(grad)
+        row_scale = np.full(n, g0 / max(count, 1) if reduction == "mean" else g0)
+    lse = np.empty(n, dtype=np.float64)
+    rows_loss = np.zeros(n, dtype=np.float64)
+    dH = np.zeros(H.shape, dtype=np.float64) if need_grad else None
+    dW = np.zeros(W.shape, dtype=np.float64) if need_grad else None
+    db = np.zeros(vocab, dtype=np.float64) if (need_grad and bias is not None) else None
+    b = None if bias is None else np.asarray(bias, dtype=np.float64)
+    for r0, r1 in _row_blocks(n, vocab):
+        z = logits(H[r0:r1], W)
+        if b is not None:
+            z = z + b[None, :]
+        lse[r0:r1] = logsumexp_rows(z)
+        for i in range(r1 - r0):
+            if valid[r0 + i]:
+                rows_loss[r0 + i] = lse[r0 + i] - z[i, y[r0 + i]]
+        if need_grad:
+            dz = _dlogits_block(z, lse[r0:r1], y[r0:r1], 1.0, ignore_index) * row_scale[r0:r1, None]
+            dH[r0:r1] = dz @ W
+            dW += dz.T @ H[r0:r1]
+            if db is not None:
+                db += dz.sum(axis=0)
+    if reduction == "none":
+        loss = rows_loss
+    elif reduction == "sum":
+        loss = float(rows_loss.sum())
+    else:
+        loss = float(rows_loss.sum()) / max(count, 1)
+    return {"lse": lse, "loss": loss, "count": count, "dH": dH, "dW": dW, "db": db}

@@ -223,3 +223,59 @@ def test_filter_special_cases():
     # a one-row-tile filtering keep their exact dH.
     f1 = oracle.forward_backward_filtered(H, W, y, 1e-3, 1, 64)
     assert np.max(np.abs(f1[2] - full[2])) <= 1e-3 * np.max(np.abs(W)) * 64 / 19
+
+
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_general_form_matches_library_cross_entropy(reduction, with_bias):
+    # Library cross-check of bias and reductions: F.linear + F.cross_entropy
+    # on explicit fp64 logits, gradients by autograd.
+    H, W, y = _rand(31, 13, 7, 29, w_scale=1.5, ignore=(2, 9))
+    b = np.random.default_rng(5).standard_normal(29) if with_bias else None
+    Ht = torch.tensor(H, requires_grad=True)
+    Wt = torch.tensor(W, requires_grad=True)
+    bt = torch.tensor(b, requires_grad=True) if with_bias else None
+    z = torch.nn.functional.linear(Ht, Wt, bt)
+    ref = torch.nn.functional.cross_entropy(z, torch.tensor(y), ignore_index=IGN, reduction=reduction)
+    if reduction == "none":
+        g = np.random.default_rng(6).standard_normal(13)
+        ref.backward(torch.tensor(g))
+    else:
+        g = -0.75
+        (ref * g).backward()
+    out = oracle.forward_backward_ex(H, W, y, bias=b, reduction=reduction, grad=g)
+    if reduction == "none":
+        assert np.max(np.abs(out["loss"] - ref.detach().numpy())) < 1e-12
+    else:
+        assert abs(out["loss"] - ref.item()) < 1e-12
+    assert np.max(np.abs(out["lse"] - torch.logsumexp(z.detach(), 1).numpy())) < 1e-12
+    assert np.max(np.abs(out["dH"] - Ht.grad.numpy())) < 1e-13
+    assert np.max(np.abs(out["dW"] - Wt.grad.numpy())) < 1e-13
+    if with_bias:
+        assert np.max(np.abs(out["db"] - bt.grad.numpy())) < 1e-13
+    else:
+        assert out["db"] is None
+
+
+def test_general_form_bias_finite_differences():
+    H, W, y = _rand(32, 5, 4, 9, w_scale=1.0, ignore=(1,))
+    b = np.random.default_rng(7).standard_normal(9)
+    out = oracle.forward_backward_ex(H, W, y, bias=b, reduction="sum", grad=1.0)
+    h = 1e-6
+    for v in range(9):
+        bp, bm = b.copy(), b.copy()
+        bp[v] += h
+        bm[v] -= h
+        fd = (oracle.forward_backward_ex(H, W, y, bias=bp, reduction="sum", need_grad=False)["loss"]
+              - oracle.forward_backward_ex(H, W, y, bias=bm, reduction="sum", need_grad=False)["loss"]) / (2 * h)
+        assert abs(fd - out["db"][v]) < 1e-6
+    # db sums dZ over rows: the columns of dZ, not its rows, so sum_v db_v = 0.
+    assert abs(out["db"].sum()) < 1e-13
+
+
+def test_general_form_reduces_to_the_plain_mean():
+    H, W, y = _rand(33, 11, 6, 17, ignore=(4,))
+    a = oracle.forward_backward_ex(H, W, y, grad=2.0)
+    lse, loss, dH, dW, _ = oracle.forward_backward(H, W, y, grad_loss=2.0)
+    assert abs(a["loss"] - loss) < 1e-14
+    assert np.max(np.abs(a["dH"] - dH)) < 1e-15 and np.max(np.abs(a["dW"] - dW)) < 1e-15
