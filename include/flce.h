@@ -83,6 +83,23 @@ typedef struct {
  * Outputs are then undefined. */
 #define FLCE_FLAG_TEST_SHORT_WAITS 0x1u
 
+/* With filter_eps > 0: apply the filter to one gradient only, as the
+ * "CCE-FullC" and "CCE-FullE" variants of Cut Cross-Entropy (Table 1, and
+ * Sec. 5.3 on pretraining) do. FULL_DW computes dW (the classifier gradient)
+ * without filtering and filters dH; FULL_DH does the opposite. */
+#define FLCE_FLAG_FILTER_FULL_DW 0x2u
+#define FLCE_FLAG_FILTER_FULL_DH 0x4u
+
+/* Remove ignored rows before the backward, as Cut Cross-Entropy suggests
+ * for masked data (App. B, "removing ignored tokens"). The forward still
+ * computes the LSE of every row. The backward then runs on the valid rows
+ * only: their H rows, targets and LSE are gathered into the workspace, and
+ * dH is scattered back, with exact zeros on ignored rows. The launch sizes
+ * depend on the valid count, so with this flag flce_forward_backward and
+ * flce_backward_ex synchronise `stream` once to read it. The workspace
+ * grows by about 6*N*D + 28*N bytes. */
+#define FLCE_FLAG_COMPACT_IGNORED 0x8u
+
 /* Bytes of device workspace the two compute calls need for problem *p
  * (0 if p is NULL or invalid). Pure host arithmetic; needs no GPU. */
 size_t flce_workspace_bytes(const flce_problem* p);
@@ -106,6 +123,34 @@ flce_status flce_forward(const flce_problem* p, const void* H, const void* W, co
 flce_status flce_forward_backward(const flce_problem* p, const void* H, const void* W, const int64_t* y,
                                   float grad_loss, float* lse, float* loss, float* dH, float* dW, void* ws,
                                   size_t ws_bytes, void* stream);
+
+/* Reductions of the per-row losses for the general entry points below. */
+#define FLCE_REDUCTION_MEAN 0 /* sum over valid rows / max(count, 1) */
+#define FLCE_REDUCTION_SUM 1  /* sum over valid rows */
+#define FLCE_REDUCTION_NONE 2 /* one loss per row, 0 on ignored rows */
+
+/* General forward: optional bias and a choice of reduction, as in the
+ * PyTorch 2.13 chapter's F.linear_cross_entropy(input, weight, target,
+ * linear_bias, ignore_index, reduction). Logits are z = H W^T + bias.
+ *   bias  fp32 [V] or NULL
+ *   lse   fp32 [N] out (required; the backward below takes it)
+ *   loss  fp32 out: [1] for MEAN and SUM, [N] for NONE
+ * No gradient is computed; pair it with flce_backward_ex. */
+flce_status flce_forward_ex(const flce_problem* p, int32_t reduction, const void* H, const void* W, const float* bias,
+                            const int64_t* y, float* lse, float* loss, void* ws, size_t ws_bytes, void* stream);
+
+/* General backward: recomputes the logits from H, W (and bias) and the LSE
+ * of flce_forward_ex, and forms dZ = s_n * (softmax - onehot) with s_n from
+ * the upstream gradient (Cut Cross-Entropy, Sec. 4.3 and Alg. 4, whose
+ * gradient is scaled per row by the backpropagated gradient of the loss).
+ *   grad   fp32 DEVICE pointer: [1] for MEAN (s_n = g / count) and SUM
+ *          (s_n = g), [N] for NONE (s_n = grad[n])
+ *   dH fp32 [N,D], dW fp32 [V,D] out (overwritten)
+ *   dbias  fp32 [V] out (overwritten) or NULL; d(bias)_v = sum_n dZ_nv
+ * With NONE, s_n multiplies G before it is rounded to bf16. */
+flce_status flce_backward_ex(const flce_problem* p, int32_t reduction, const void* H, const void* W,
+                             const float* bias, const int64_t* y, const float* lse, const float* grad, float* dH,
+                             float* dW, float* dbias, void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, returns the device status word of the most recent
  * call that used `ws` (FLCE_OK, FLCE_ERR_BAD_TARGET or FLCE_ERR_TIMEOUT; the
@@ -162,6 +207,8 @@ flce_status flce_forward_static_scratch(const flce_problem* p, const void* H, co
 #define FLCE_KERNEL_FINALIZE 6
 #define FLCE_KERNEL_FILTER_STATS 7
 #define FLCE_KERNEL_GEMM_BWD 8 /* one launch: dW and dH of a chunk + dZ of the next chunk */
+#define FLCE_KERNEL_DBIAS 9
+#define FLCE_KERNEL_SET_SCALE 10
 flce_status flce_profile_set(void** events, int32_t* kinds, int32_t cap);
 int32_t flce_profile_count(void);
 

@@ -6,14 +6,20 @@ fails when the library has not been built: there is no CPU fallback.
 """
 
 from ._binding import (  # noqa: F401
+    FLAG_COMPACT_IGNORED,
+    FLAG_FILTER_FULL_DH,
+    FLAG_FILTER_FULL_DW,
     FLAG_TEST_SHORT_WAITS,
+    REDUCTIONS,
     FlceError,
     FlceProblem,
     LaunchProfiler,
     Status,
     declared_symbols,
     flce_forward,
+    flce_backward_ex,
     flce_forward_backward,
+    flce_forward_ex,
     flce_forward_static_scratch,
     flce_get_device_status,
     flce_get_filter_stats,
@@ -23,3 +29,4 @@ from ._binding import (  # noqa: F401
     make_problem,
 )
 from .api import Workspace, device_status, forward, forward_backward  # noqa: F401
+from .autograd import FusedLinearCrossEntropy, linear_cross_entropy  # noqa: F401

@@ -29,6 +29,10 @@ class Status(enum.IntEnum):
 
 
 FLAG_TEST_SHORT_WAITS = 0x1
+FLAG_FILTER_FULL_DW = 0x2
+FLAG_FILTER_FULL_DH = 0x4
+FLAG_COMPACT_IGNORED = 0x8
+REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 
 class FlceError(RuntimeError):
@@ -72,6 +76,10 @@ def _load() -> ctypes.CDLL:
     lib.flce_status_string.restype = ctypes.c_char_p
     lib.flce_get_filter_stats.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_double)]
     lib.flce_get_filter_stats.restype = ctypes.c_int
+    lib.flce_forward_ex.argtypes = [prob, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.flce_forward_ex.restype = ctypes.c_int
+    lib.flce_backward_ex.argtypes = [prob, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.flce_backward_ex.restype = ctypes.c_int
     lib.flce_forward_static_scratch.argtypes = [prob, vp, vp, vp, vp, vp, vp]
     lib.flce_forward_static_scratch.restype = ctypes.c_int
     lib.flce_profile_set.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]
@@ -130,6 +138,22 @@ def flce_forward_backward(problem, H, W, y, grad_loss: float, lse, loss, dH, dW,
                                             _addr(dH), _addr(dW), _addr(ws), nb, _stream(stream)))
 
 
+def flce_forward_ex(problem, reduction: int, H, W, bias, y, lse, loss, ws, ws_bytes: int | None = None,
+                    stream=None) -> Status:
+    nb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    return Status(lib.flce_forward_ex(ctypes.byref(problem) if problem is not None else None, int(reduction),
+                                      _addr(H), _addr(W), _addr(bias), _addr(y), _addr(lse), _addr(loss), _addr(ws),
+                                      nb, _stream(stream)))
+
+
+def flce_backward_ex(problem, reduction: int, H, W, bias, y, lse, grad, dH, dW, dbias, ws,
+                     ws_bytes: int | None = None, stream=None) -> Status:
+    nb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    return Status(lib.flce_backward_ex(ctypes.byref(problem) if problem is not None else None, int(reduction),
+                                       _addr(H), _addr(W), _addr(bias), _addr(y), _addr(lse), _addr(grad),
+                                       _addr(dH), _addr(dW), _addr(dbias), _addr(ws), nb, _stream(stream)))
+
+
 def flce_forward_static_scratch(problem, H, W, y, lse, loss, stream=None) -> Status:
     """flce_forward for callers that cannot hand over a workspace (no device
     allocation at call time); its scratch is a fixed 16 MiB array inside the
@@ -155,7 +179,7 @@ def flce_get_filter_stats(ws, stream=None) -> float:
 
 
 KERNEL_KINDS = {0: "gemm_lse", 1: "gemm_dz", 2: "gemm_dw", 3: "gemm_dh", 4: "prep", 5: "combine",
-                6: "finalize", 7: "filter_stats", 8: "gemm_bwd"}
+                6: "finalize", 7: "filter_stats", 8: "gemm_bwd", 9: "dbias", 10: "set_scale"}
 
 
 class LaunchProfiler:

@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libflce.so")
 SOURCES = [os.path.join(CSRC, "flce.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, "tile_gemm.cuh"), os.path.join(CSRC, "ptx_sm103.cuh"),
+DEPENDS = SOURCES + [os.path.join(CSRC, "tile_gemm.cuh"), os.path.join(CSRC, "tile_gemm_pair.cuh"),
+                     os.path.join(CSRC, "ptx_sm103.cuh"),
                      os.path.join(INCLUDE, "flce.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -25,14 +25,17 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "flce.h"
 #include "tile_gemm.cuh"
+#include "tile_gemm_pair.cuh"
 
 namespace flce {
 
 constexpr int kRowChunk = 8192;    // rows per chunk (multiple of 256)
-constexpr int kVocabChunk = 8192;  // vocabulary ids per backward chunk (multiple of 256)
+constexpr int kVocabChunkMin = 4096;   // candidate vocabulary chunks of the backward (multiples of 256);
+constexpr int kVocabChunkMax = 10240;  // the workspace is sized for the largest
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kShortWaitNs = 1000ull;
 
@@ -109,7 +112,7 @@ __global__ void __launch_bounds__(kCombineRows * kCombineSplit)
     lse_combine_kernel(const float* __restrict__ part_m, const float* __restrict__ part_s, int part_ld, int n_tiles,
                        const float* __restrict__ zy, const int64_t* __restrict__ y, int64_t row0, int rows,
                        int64_t vocab, int64_t ignore_index, float* __restrict__ lse_out,
-                       double* __restrict__ block_sums) {
+                       double* __restrict__ block_sums, float* __restrict__ loss_rows) {
   __shared__ float sh_m[kCombineSplit][kCombineRows];
   __shared__ float sh_s[kCombineSplit][kCombineRows];
   __shared__ double red[kCombineRows];
@@ -131,6 +134,7 @@ __global__ void __launch_bounds__(kCombineRows * kCombineSplit)
       lse_out[row0 + lr] = lse;
       const int64_t t = y[row0 + lr];
       if (t != ignore_index && t >= 0 && t < vocab) contrib = (double)lse - (double)zy[lr];
+      if (loss_rows) loss_rows[row0 + lr] = (float)contrib;
     }
     red[r] = contrib;
   }
@@ -145,7 +149,7 @@ __global__ void __launch_bounds__(kCombineRows * kCombineSplit)
 // One block: fixed-order fp64 sum of the per-block row losses, mean over the
 // valid count (clamped to one), and the gradient scale g / count.
 __global__ void finalize_kernel(const double* __restrict__ block_sums, int n_blocks, float grad_loss, WsHeader* hdr,
-                                float* loss_out) {
+                                float* loss_out, int reduction) {
   __shared__ double red[256];
   double acc = 0.0;
   for (int i = threadIdx.x; i < n_blocks; i += 256) acc += block_sums[i];
@@ -156,11 +160,43 @@ __global__ void finalize_kernel(const double* __restrict__ block_sums, int n_blo
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    const double denom = (double)(hdr->count > 0 ? hdr->count : 1);
+    // reduction 0 = mean over the valid count (clamped to 1), 1 = sum, 2 = none
+    const double denom = reduction == 0 ? (double)(hdr->count > 0 ? hdr->count : 1) : 1.0;
     const float loss = (float)(red[0] / denom);
     hdr->loss = loss;
-    hdr->scale = (float)((double)grad_loss / denom);
-    *loss_out = loss;
+    hdr->scale = reduction == 2 ? 1.0f : (float)((double)grad_loss / denom);
+    if (reduction != 2) *loss_out = loss;
+  }
+}
+
+// Gradient scale of a backward whose upstream gradient lives on the device:
+// g / max(count, 1) for a mean, g for a sum, 1 for per-row gradients (they
+// scale G inside the dZ epilogue).
+__global__ void set_scale_kernel(const float* __restrict__ grad, int reduction, WsHeader* hdr) {
+  if (threadIdx.x == 0) {
+    const double denom = reduction == 0 ? (double)(hdr->count > 0 ? hdr->count : 1) : 1.0;
+    hdr->scale = reduction == 2 ? 1.0f : (float)((double)grad[0] / denom);
+  }
+}
+
+// d(bias) of one staging chunk: out[c] (=|+=) scale * sum over the chunk's
+// rows of G[r][c]. A block covers 32 columns; thread (c, g) sums rows g,
+// g + 8, ... and the 8 partial sums are added in g order (fixed order).
+__global__ void __launch_bounds__(256) dbias_chunk_kernel(const __nv_bfloat16* __restrict__ stage, int ld, int rows,
+                                                          int cols, const float* __restrict__ scale,
+                                                          float* __restrict__ out, int accumulate) {
+  __shared__ float part[8][32];
+  const int c = blockIdx.x * 32 + threadIdx.x, g = threadIdx.y;
+  float acc = 0.f;
+  if (c < cols)
+    for (int r = g; r < rows; r += 8) acc += __bfloat162float(stage[(size_t)r * ld + c]);
+  part[g][threadIdx.x] = acc;
+  __syncthreads();
+  if (g == 0 && c < cols) {
+    float t = 0.f;
+    for (int k = 0; k < 8; ++k) t += part[k][threadIdx.x];
+    t *= __ldg(scale);
+    out[c] = accumulate ? out[c] + t : t;
   }
 }
 
@@ -182,6 +218,69 @@ __global__ void count_skipped_kernel(const uint32_t* __restrict__ flags, int row
     atomicAdd(&hdr->tiles_total, (unsigned long long)(rows * cols));
     atomicAdd(&hdr->tiles_skipped, (unsigned long long)red[0]);
   }
+}
+
+// Ignored-row compaction, one block: idx[i] = original row of the i-th
+// valid row (order kept), pos[n] = compact position of row n or -1. Thread t
+// owns a contiguous segment of rows; segment counts are scanned in order.
+__global__ void __launch_bounds__(1024) compact_index_kernel(const int64_t* __restrict__ y, int64_t n, int64_t vocab,
+                                                             int64_t ignore_index, int32_t* __restrict__ idx,
+                                                             int32_t* __restrict__ pos) {
+  __shared__ int32_t offs[1024];
+  const int64_t seg = (n + blockDim.x - 1) / blockDim.x;
+  const int64_t r0 = threadIdx.x * seg, r1 = min(n, r0 + seg);
+  int32_t c = 0;
+  for (int64_t r = r0; r < r1; ++r) {
+    const int64_t t = y[r];
+    c += (t != ignore_index && t >= 0 && t < vocab) ? 1 : 0;
+  }
+  offs[threadIdx.x] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int32_t run = 0;
+    for (int i = 0; i < (int)blockDim.x; ++i) {
+      const int32_t v = offs[i];
+      offs[i] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  int32_t o = offs[threadIdx.x];
+  for (int64_t r = r0; r < r1; ++r) {
+    const int64_t t = y[r];
+    if (t != ignore_index && t >= 0 && t < vocab) {
+      idx[o] = (int32_t)r;
+      pos[r] = o++;
+    } else {
+      pos[r] = -1;
+    }
+  }
+}
+
+// Row i of the compacted problem: H row, target, LSE and (optional) row
+// scale of original row idx[i]. One block per compact row.
+__global__ void gather_rows_kernel(const uint4* __restrict__ H, int row_vec, const int32_t* __restrict__ idx,
+                                   int64_t count, uint4* __restrict__ Hc, const int64_t* __restrict__ y,
+                                   int64_t* __restrict__ yc, const float* __restrict__ lse, float* __restrict__ lsec,
+                                   const float* __restrict__ rs, float* __restrict__ rsc) {
+  const int64_t i = blockIdx.x;
+  if (i >= count) return;
+  const int64_t r = idx[i];
+  for (int k = threadIdx.x; k < row_vec; k += blockDim.x) Hc[i * row_vec + k] = H[r * row_vec + k];
+  if (threadIdx.x == 0) {
+    yc[i] = y[r];
+    lsec[i] = lse[r];
+    if (rs) rsc[i] = rs[r];
+  }
+}
+
+// dH row n = compacted dH row pos[n], or zeros for an ignored row.
+__global__ void scatter_rows_kernel(const float4* __restrict__ dHc, int row_vec, const int32_t* __restrict__ pos,
+                                    float4* __restrict__ dH) {
+  const int64_t n = blockIdx.x;
+  const int32_t p = pos[n];
+  for (int k = threadIdx.x; k < row_vec; k += blockDim.x)
+    dH[n * row_vec + k] = p >= 0 ? dHc[(int64_t)p * row_vec + k] : make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // ------------------------------------------------------------------ host side
@@ -217,10 +316,14 @@ static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 struct Plan {
   int64_t n, d, v;
-  int nc, vc;            // row and vocabulary chunk sizes
+  int nc, vc;            // row chunk; vocabulary chunk the workspace is sized for
+  int vcu;               // vocabulary chunk the backward uses (<= vc)
   int n_vtiles;          // ceil(V / 256)
   int row_chunks, v_chunks;
-  size_t off_pm, off_ps, off_zy, off_lse, off_bsum, off_flags[2], off_stage[2], total;
+  size_t off_pm, off_ps, off_zy, off_lse, off_bsum, off_flags[2], off_stage[2];
+  // ignored-row compaction (FLCE_FLAG_COMPACT_IGNORED only)
+  size_t off_cidx, off_cpos, off_hc, off_dhc, off_yc, off_lsec, off_rsc;
+  size_t total;
 };
 
 // Workspace layout for a row chunk of nc rows (a multiple of 256).
@@ -230,10 +333,11 @@ static Plan make_plan_rows(const flce_problem& p, int nc) {
   pl.d = p.hidden;
   pl.v = p.vocab;
   pl.nc = nc;
-  pl.vc = (int)std::min<int64_t>(align_up((size_t)p.vocab, 256), kVocabChunk);
+  pl.vc = (int)std::min<int64_t>(align_up((size_t)p.vocab, 256), kVocabChunkMax);
   pl.n_vtiles = (int)ceil_div(p.vocab, kBN);
   pl.row_chunks = (int)ceil_div(std::max<int64_t>(p.n_rows, 1), pl.nc);
-  pl.v_chunks = (int)ceil_div(p.vocab, pl.vc);
+  pl.vcu = pl.vc;
+  pl.v_chunks = (int)ceil_div(p.vocab, pl.vcu);
   size_t off = align_up(sizeof(WsHeader), 1024);
   pl.off_pm = off;
   off = align_up(off + (size_t)pl.n_vtiles * pl.nc * 4, 1024);
@@ -253,8 +357,97 @@ static Plan make_plan_rows(const flce_problem& p, int nc) {
     pl.off_stage[b] = off;
     off = align_up(off + (size_t)pl.nc * pl.vc * 2, 1024);
   }
+  if (p.flags & FLCE_FLAG_COMPACT_IGNORED) {
+    const size_t n = (size_t)std::max<int64_t>(p.n_rows, 1), d = (size_t)p.hidden;
+    pl.off_cidx = off;
+    off = align_up(off + n * 4, 1024);
+    pl.off_cpos = off;
+    off = align_up(off + n * 4, 1024);
+    pl.off_hc = off;
+    off = align_up(off + n * d * 2, 1024);
+    pl.off_dhc = off;
+    off = align_up(off + n * d * 4, 1024);
+    pl.off_yc = off;
+    off = align_up(off + n * 8, 1024);
+    pl.off_lsec = off;
+    off = align_up(off + n * 4, 1024);
+    pl.off_rsc = off;
+    off = align_up(off + n * 4, 1024);
+  }
   pl.total = off;
   return pl;
+}
+
+// Predicted makespan, in 64-deep k-blocks, of the backward launches for a
+// vocabulary chunk of vc ids: each launch assigns its tile groups to `slots`
+// persistent CTAs (or CTA pairs) round-robin, so a launch lasts as long as its
+// busiest slot; `launch_cost` charges each launch's ramp-up and drain.
+static double predict_backward(const flce_problem& p, int nc, int vc, int slots, int cluster) {
+  const int64_t d_tiles = ceil_div(p.hidden, kBN), kd = ceil_div(p.hidden, kBK);
+  const double launch_cost = 24.0;
+  std::vector<int64_t> load(slots);
+  int64_t next = 0;    // index of the next unit in the current launch
+  double total = 0.0;
+  auto add = [&](int64_t units, int64_t cost) {
+    if (units <= 0) return;
+    const int64_t full = units / slots, rem = units % slots;
+    for (int c = 0; c < slots; ++c) {
+      const int64_t k = (c - next % slots + slots) % slots;   // slot c's position after `next`
+      load[c] += (full + (k < rem ? 1 : 0)) * cost;
+    }
+    next += units;
+  };
+  auto close = [&]() {
+    total += (double)*std::max_element(load.begin(), load.end()) + launch_cost;
+    std::fill(load.begin(), load.end(), 0);
+    next = 0;
+  };
+  auto groups = [&](int64_t m_tiles) { return ceil_div(m_tiles, cluster); };
+  const int64_t rcs = ceil_div(std::max<int64_t>(p.n_rows, 1), nc), vcs = ceil_div(p.vocab, vc);
+  auto dz_units = [&](int64_t s, int64_t& units) {
+    const int64_t rows = std::min<int64_t>(nc, p.n_rows - (s / vcs) * nc);
+    const int64_t cols = std::min<int64_t>(vc, p.vocab - (s % vcs) * vc);
+    units = groups(ceil_div(rows, kBM)) * ceil_div(cols, kBN);
+  };
+  int64_t u;
+  dz_units(0, u);
+  add(u, kd);
+  close();
+  for (int64_t s = 0; s < rcs * vcs; ++s) {
+    const int64_t rows = std::min<int64_t>(nc, p.n_rows - (s / vcs) * nc);
+    const int64_t cols = std::min<int64_t>(vc, p.vocab - (s % vcs) * vc);
+    add(groups(ceil_div(cols, kBM)) * d_tiles, ceil_div(rows, kBK));   // dW
+    add(groups(ceil_div(rows, kBM)) * d_tiles, ceil_div(cols, kBK));   // dH
+    if (s + 1 < rcs * vcs) {
+      dz_units(s + 1, u);
+      add(u, kd);
+    }
+    close();
+  }
+  return total;
+}
+
+// The vocabulary chunk (a multiple of 256, at most the allocated one) with
+// the smallest predicted backward makespan; ties go to the larger chunk.
+static int choose_vocab_chunk(const flce_problem& p, int nc, int vc_alloc, int slots, int cluster) {
+  static std::mutex mu;
+  static int64_t key[6] = {-1, -1, -1, -1, -1, -1};
+  static int cached = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  const int64_t k[6] = {p.n_rows, p.hidden, p.vocab, nc, slots, cluster};
+  if (std::equal(k, k + 6, key)) return std::min(cached, vc_alloc);
+  int best = vc_alloc;
+  double best_t = predict_backward(p, nc, vc_alloc, slots, cluster);
+  for (int vc = vc_alloc - 256; vc >= std::min(kVocabChunkMin, vc_alloc); vc -= 256) {
+    const double t = predict_backward(p, nc, vc, slots, cluster);
+    if (t < best_t * 0.9999) {
+      best_t = t;
+      best = vc;
+    }
+  }
+  std::copy(k, k + 6, key);
+  cached = best;
+  return best;
 }
 
 static Plan make_plan(const flce_problem& p) {
@@ -267,7 +460,9 @@ static bool problem_ok(const flce_problem* p) {
   if (p->hidden < 1 || p->hidden > (int64_t)1 << 20) return false;
   if (p->vocab < 1 || p->vocab >= (int64_t)1 << 31) return false;
   if (!(p->filter_eps >= 0.f) || !std::isfinite(p->filter_eps)) return false;
-  if ((p->flags & ~FLCE_FLAG_TEST_SHORT_WAITS) != 0u) return false;
+  if ((p->flags & ~(FLCE_FLAG_TEST_SHORT_WAITS | FLCE_FLAG_FILTER_FULL_DW | FLCE_FLAG_FILTER_FULL_DH |
+                    FLCE_FLAG_COMPACT_IGNORED)) != 0u)
+    return false;
   return true;
 }
 
@@ -321,6 +516,9 @@ static bool device_setup(int* sms_out) {
     if (cudaFuncSetAttribute(flce_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kGemmSmemBytes) != cudaSuccess)
       return false;
+    if (cudaFuncSetAttribute(flce_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kPairSmemBytes) != cudaSuccess)
+      return false;
     info[dev].sms = sms;
     info[dev].ready = true;
   }
@@ -328,22 +526,42 @@ static bool device_setup(int* sms_out) {
   return true;
 }
 
-// CTAs per cluster of the GEMM launches: 1 (independent CTAs) unless
-// FLCE_GEMM_CLUSTER=2 asks for pairs that share the B tile through TMA multicast.
-static int gemm_cluster() {
-  static int kc = [] {
-    const char* e = std::getenv("FLCE_GEMM_CLUSTER");
-    return (e && std::atoi(e) == 2) ? 2 : 1;
+// Kernel variant of the GEMM launches:
+//   GEMM_CTA1       one CTA per tile, each loading its own A and B;
+//   GEMM_MULTICAST  2-CTA clusters on vertically adjacent tiles sharing the B
+//                   tile through TMA multicast;
+//   GEMM_PAIR       2-CTA clusters issuing tcgen05.mma.cta_group::2 (M = 256).
+// GEMM_PAIR is the default; FLCE_GEMM_MODE=cta1|multicast|pair overrides it.
+// Launches that skip filtered k-blocks always use GEMM_CTA1 (the others
+// compute both halves of a group together).
+enum GemmMode { GEMM_CTA1 = 1, GEMM_MULTICAST = 2, GEMM_PAIR = 3 };
+
+static GemmMode gemm_mode() {
+  static GemmMode mode = [] {
+    const char* e = std::getenv("FLCE_GEMM_MODE");
+    if (e && std::strcmp(e, "multicast") == 0) return GEMM_MULTICAST;
+    if (e && std::strcmp(e, "cta1") == 0) return GEMM_CTA1;
+    return GEMM_PAIR;
   }();
-  return kc;
+  return mode;
+}
+
+// Kernel variant of the backward launches, and the vocabulary chunk they use.
+static GemmMode backward_mode(const flce_problem& p) { return p.filter_eps > 0.f ? GEMM_CTA1 : gemm_mode(); }
+
+static void choose_backward_chunk(Plan& pl, const flce_problem& p, int sms) {
+  const int cluster = backward_mode(p) == GEMM_CTA1 ? 1 : 2;
+  pl.vcu = choose_vocab_chunk(p, pl.nc, pl.vc, std::max(1, sms / cluster), cluster);
+  pl.v_chunks = (int)ceil_div(p.vocab, pl.vcu);
 }
 
 // Collects up to kMaxProblems GEMM problems for one persistent launch.
 struct Group {
   GemmLaunch L;
   int units = 0;
+  GemmMode mode;
   int cluster;
-  explicit Group(int kc) : cluster(kc) { std::memset(&L, 0, sizeof(L)); }
+  explicit Group(GemmMode m) : mode(m), cluster(m == GEMM_CTA1 ? 1 : 2) { std::memset(&L, 0, sizeof(L)); }
   void add(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& out, const GemmParams& gp) {
     const int u = (int)ceil_div(gp.m_tiles, cluster) * gp.n_tiles;
     if (u <= 0) return;
@@ -360,7 +578,7 @@ struct Group {
 static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
   if (g.units <= 0) return true;
   ProfScope prof(kind, st);
-  if (g.cluster == 1) {
+  if (g.mode == GEMM_CTA1) {
     const int grid = std::min(g.units, sms);
     flce_gemm_kernel<1><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(g.L);
     return cudaGetLastError() == cudaSuccess;
@@ -370,7 +588,7 @@ static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = kGemmSmemBytes;
+  cfg.dynamicSmemBytes = g.mode == GEMM_PAIR ? kPairSmemBytes : kGemmSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -379,6 +597,7 @@ static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (g.mode == GEMM_PAIR) return cudaLaunchKernelEx(&cfg, flce_gemm_pair_kernel, g.L) == cudaSuccess;
   return cudaLaunchKernelEx(&cfg, flce_gemm_kernel<2>, g.L) == cudaSuccess;
 }
 
@@ -399,8 +618,10 @@ static GemmParams base_params(const flce_problem& p, WsHeader* hdr) {
 }
 
 // prep + forward GEMM + combine per row chunk + finalize.
+// reduction: 0 mean, 1 sum, 2 none (per-row losses into loss_rows, `loss` unused).
 static flce_status run_forward(const flce_problem& p, const Plan& pl, const Maps& mp, const int64_t* y,
-                               float* lse, float* loss, float grad_loss, uint8_t* ws, int sms, cudaStream_t st) {
+                               float* lse, float* loss, float grad_loss, uint8_t* ws, int sms, cudaStream_t st,
+                               const float* bias = nullptr, int reduction = 0, float* loss_rows = nullptr) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   float* part_m = reinterpret_cast<float*>(ws + pl.off_pm);
   float* part_s = reinterpret_cast<float*>(ws + pl.off_ps);
@@ -431,18 +652,19 @@ static flce_status run_forward(const flce_problem& p, const Plan& pl, const Maps
     gp.part_m = part_m;
     gp.part_s = part_s;
     gp.zy = zy;
-    const int kc = gemm_cluster();
-    Group g(kc);
-    g.add(mp.h_k, kc == 1 ? mp.w_k : mp.w_k_half, mp.h_k, gp);
+    gp.bias = bias;
+    const GemmMode gm = gemm_mode();
+    Group g(gm);
+    g.add(mp.h_k, gm == GEMM_CTA1 ? mp.w_k : mp.w_k_half, mp.h_k, gp);
     if (!launch_group(FLCE_KERNEL_GEMM_LSE, g, sms, st)) return FLCE_ERR_CUDA;
     ProfScope prof(FLCE_KERNEL_COMBINE, st);
     lse_combine_kernel<<<(int)ceil_div(rows, kCombineRows), dim3(kCombineRows, kCombineSplit), 0, st>>>(
-        part_m, part_s, pl.nc, pl.n_vtiles, zy, y, r0, rows, p.vocab, p.ignore_index, lse, bsum);
+        part_m, part_s, pl.nc, pl.n_vtiles, zy, y, r0, rows, p.vocab, p.ignore_index, lse, bsum, loss_rows);
     if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
   }
   const int n_blocks = (int)ceil_div(p.n_rows, kCombineRows);
   ProfScope prof(FLCE_KERNEL_FINALIZE, st);
-  finalize_kernel<<<1, 256, 0, st>>>(bsum, n_blocks, grad_loss, hdr, loss);
+  finalize_kernel<<<1, 256, 0, st>>>(bsum, n_blocks, grad_loss, hdr, loss, reduction);
   if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
   return FLCE_OK;
 }
@@ -451,7 +673,8 @@ static flce_status run_forward(const flce_problem& p, const Plan& pl, const Maps
 // stages its dZ in buffer s % 2. The dZ GEMM of item s+1 shares a launch with
 // the dW and dH GEMMs of item s: they touch different staging buffers.
 static flce_status run_backward(const flce_problem& p, const Plan& pl, const Maps& mp, const int64_t* y,
-                                const float* lse, uint8_t* ws, int sms, cudaStream_t st) {
+                                const float* lse, uint8_t* ws, int sms, cudaStream_t st, const float* bias = nullptr,
+                                const float* row_scale = nullptr, float* dbias = nullptr) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int filter = p.filter_eps > 0.f ? 1 : 0;
   const int d_tiles = (int)ceil_div(p.hidden, kBN);
@@ -460,8 +683,8 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     const int rc = s / pl.v_chunks, vi = s % pl.v_chunks;
     r0 = (int64_t)rc * pl.nc;
     rows = (int)std::min<int64_t>(pl.nc, p.n_rows - r0);
-    v0 = (int64_t)vi * pl.vc;
-    cols = (int)std::min<int64_t>(pl.vc, p.vocab - v0);
+    v0 = (int64_t)vi * pl.vcu;
+    cols = (int)std::min<int64_t>(pl.vcu, p.vocab - v0);
   };
   auto dz_params = [&](int s) {
     int64_t r0, v0;
@@ -482,9 +705,25 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     dz.lse = lse;
     dz.filter = filter;
     dz.filter_eps = p.filter_eps;
+    dz.bias = bias;
+    dz.row_scale = row_scale;
     dz.flags = reinterpret_cast<uint32_t*>(ws + pl.off_flags[s & 1]);
-    dz.flags_ld = pl.vc / kBN;
+    dz.flags_ld = pl.vcu / kBN;
     return dz;
+  };
+  // d(bias) of item s, read from its staging buffer before that buffer is
+  // overwritten two items later.
+  auto dbias_item = [&](int s) -> bool {
+    if (!dbias) return true;
+    int64_t r0, v0;
+    int rows, cols;
+    item_geom(s, r0, rows, v0, cols);
+    const int rc = s / pl.v_chunks;
+    const __nv_bfloat16* stage = reinterpret_cast<const __nv_bfloat16*>(ws + pl.off_stage[s & 1]);
+    ProfScope prof(FLCE_KERNEL_DBIAS, st);
+    dbias_chunk_kernel<<<(int)ceil_div(cols, 32), dim3(32, 8), 0, st>>>(stage, pl.vcu, rows, cols, &hdr->scale,
+                                                                        dbias + v0, rc > 0 ? 1 : 0);
+    return cudaGetLastError() == cudaSuccess;
   };
   auto count_skipped = [&](const GemmParams& dz) -> bool {
     if (!filter) return true;
@@ -493,14 +732,15 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     return cudaGetLastError() == cudaSuccess;
   };
 
-  const int kc = gemm_cluster();
-  const CUtensorMap& w_b = kc == 1 ? mp.w_k : mp.w_k_half;
+  const GemmMode gm = backward_mode(p);
+  const CUtensorMap& w_b = gm == GEMM_CTA1 ? mp.w_k : mp.w_k_half;
   {
-    Group g(kc);
+    Group g(gm);
     const GemmParams dz0 = dz_params(0);
     g.add(mp.h_k, w_b, mp.s_store[0], dz0);
     if (!launch_group(FLCE_KERNEL_GEMM_DZ, g, sms, st)) return FLCE_ERR_CUDA;
     if (!count_skipped(dz0)) return FLCE_ERR_CUDA;
+    if (!dbias_item(0)) return FLCE_ERR_CUDA;
   }
   for (int s = 0; s < items; ++s) {
     const int b = s & 1;
@@ -509,7 +749,7 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     item_geom(s, r0, rows, v0, cols);
     const int rc = s / pl.v_chunks, vi = s % pl.v_chunks;
     uint32_t* flags = reinterpret_cast<uint32_t*>(ws + pl.off_flags[b]);
-    Group g(kc);
+    Group g(gm);
     // dW[v0 : v0+cols, :] (=|+=) scale * staging^T * H[r0 : r0+rows, :]
     GemmParams dw = base_params(p, hdr);
     dw.m_tiles = (int)ceil_div(cols, kBM);
@@ -522,9 +762,9 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     dw.mode = rc == 0 ? EPI_STORE : EPI_REDUCE;
     dw.out_m0 = (int32_t)v0;
     dw.scale = &hdr->scale;
-    dw.skip_by_flags = filter;
+    dw.skip_by_flags = filter && !(p.flags & FLCE_FLAG_FILTER_FULL_DW);
     dw.flags = flags;
-    dw.flags_ld = pl.vc / kBN;
+    dw.flags_ld = pl.vcu / kBN;
     dw.flags_a_is_rows = 0;
     g.add(mp.s_mn[b], mp.h_mn, mp.dw, dw);
     // dH[r0 : r0+rows, :] (=|+=) scale * staging * W[v0 : v0+cols, :]
@@ -539,9 +779,9 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     dh.mode = vi == 0 ? EPI_STORE : EPI_REDUCE;
     dh.out_m0 = (int32_t)r0;
     dh.scale = &hdr->scale;
-    dh.skip_by_flags = filter;
+    dh.skip_by_flags = filter && !(p.flags & FLCE_FLAG_FILTER_FULL_DH);
     dh.flags = flags;
-    dh.flags_ld = pl.vc / kBN;
+    dh.flags_ld = pl.vcu / kBN;
     dh.flags_a_is_rows = 1;
     g.add(mp.s_k[b], mp.w_mn, mp.dh, dh);
     GemmParams dz_next;
@@ -552,9 +792,16 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     }
     if (!launch_group(FLCE_KERNEL_GEMM_BWD, g, sms, st)) return FLCE_ERR_CUDA;
     if (has_next && !count_skipped(dz_next)) return FLCE_ERR_CUDA;
+    if (has_next && !dbias_item(s + 1)) return FLCE_ERR_CUDA;
   }
   return FLCE_OK;
 }
+
+// The backward, with ignored rows removed first when the problem asks for it.
+static flce_status run_backward_any(const flce_problem& p, const Plan& pl, const Maps& mp, const void* H,
+                                    const void* W, const int64_t* y, const float* lse, float* dH, float* dW,
+                                    uint8_t* ws, int sms, cudaStream_t st, const float* bias, const float* row_scale,
+                                    float* dbias);
 
 static bool build_maps(const flce_problem& p, const Plan& pl, const void* H, const void* W, float* dH, float* dW,
                        uint8_t* ws, bool backward, Maps* mp) {
@@ -568,7 +815,7 @@ static bool build_maps(const flce_problem& p, const Plan& pl, const void* H, con
   if (!make_map(&mp->w_mn, bf, W, D, V, D * 2, 64, 64)) return false;
   for (int b = 0; b < 2; ++b) {
     void* stage = ws + pl.off_stage[b];
-    const uint64_t vc = (uint64_t)pl.vc, nc = (uint64_t)pl.nc;
+    const uint64_t vc = (uint64_t)pl.vcu, nc = (uint64_t)pl.nc;
     if (!make_map(&mp->s_store[b], bf, stage, vc, nc, vc * 2, 64, 32)) return false;
     if (!make_map(&mp->s_k[b], bf, stage, vc, nc, vc * 2, 64, kBM)) return false;
     if (!make_map(&mp->s_mn[b], bf, stage, vc, nc, vc * 2, 64, 64)) return false;
@@ -576,6 +823,50 @@ static bool build_maps(const flce_problem& p, const Plan& pl, const void* H, con
   if (!make_map(&mp->dh, f32, dH, D, N, D * 4, 32, 32)) return false;
   if (!make_map(&mp->dw, f32, dW, D, V, D * 4, 32, 32)) return false;
   return true;
+}
+
+static flce_status run_backward_any(const flce_problem& p, const Plan& pl, const Maps& mp, const void* H,
+                                    const void* W, const int64_t* y, const float* lse, float* dH, float* dW,
+                                    uint8_t* ws, int sms, cudaStream_t st, const float* bias, const float* row_scale,
+                                    float* dbias) {
+  if (!(p.flags & FLCE_FLAG_COMPACT_IGNORED))
+    return run_backward(p, pl, mp, y, lse, ws, sms, st, bias, row_scale, dbias);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  int32_t* idx = reinterpret_cast<int32_t*>(ws + pl.off_cidx);
+  int32_t* pos = reinterpret_cast<int32_t*>(ws + pl.off_cpos);
+  compact_index_kernel<<<1, 1024, 0, st>>>(y, p.n_rows, p.vocab, p.ignore_index, idx, pos);
+  if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  // The valid count sizes every launch below: read it back (one synchronisation).
+  int64_t count = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (cudaMemcpy(&count, &hdr->count, sizeof(count), cudaMemcpyDeviceToHost) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (count == p.n_rows) return run_backward(p, pl, mp, y, lse, ws, sms, st, bias, row_scale, dbias);
+  if (count == 0) {
+    if (cudaMemsetAsync(dH, 0, (size_t)p.n_rows * p.hidden * 4, st) != cudaSuccess) return FLCE_ERR_CUDA;
+    if (cudaMemsetAsync(dW, 0, (size_t)p.vocab * p.hidden * 4, st) != cudaSuccess) return FLCE_ERR_CUDA;
+    if (dbias && cudaMemsetAsync(dbias, 0, (size_t)p.vocab * 4, st) != cudaSuccess) return FLCE_ERR_CUDA;
+    return FLCE_OK;
+  }
+  void* Hc = ws + pl.off_hc;
+  float* dHc = reinterpret_cast<float*>(ws + pl.off_dhc);
+  int64_t* yc = reinterpret_cast<int64_t*>(ws + pl.off_yc);
+  float* lsec = reinterpret_cast<float*>(ws + pl.off_lsec);
+  float* rsc = row_scale ? reinterpret_cast<float*>(ws + pl.off_rsc) : nullptr;
+  gather_rows_kernel<<<(unsigned)count, 256, 0, st>>>(static_cast<const uint4*>(H), (int)(p.hidden / 8), idx, count,
+                                                      static_cast<uint4*>(Hc), y, yc, lse, lsec, row_scale, rsc);
+  if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  flce_problem pc = p;
+  pc.n_rows = count;
+  pc.flags &= ~FLCE_FLAG_COMPACT_IGNORED;
+  Plan plc = make_plan(pc);   // fits in front of the compaction buffers: plc.total <= pl.off_cidx
+  choose_backward_chunk(plc, pc, sms);
+  Maps mpc;
+  if (!build_maps(pc, plc, Hc, W, dHc, dW, ws, true, &mpc)) return FLCE_ERR_CUDA;
+  flce_status r = run_backward(pc, plc, mpc, yc, lsec, ws, sms, st, bias, rsc, dbias);
+  if (r != FLCE_OK) return r;
+  scatter_rows_kernel<<<(unsigned)p.n_rows, 256, 0, st>>>(reinterpret_cast<const float4*>(dHc), (int)(p.hidden / 4),
+                                                          pos, reinterpret_cast<float4*>(dH));
+  return cudaGetLastError() == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
 }
 
 static flce_status check_common(const flce_problem* p, const void* H, const void* W, const int64_t* y,
@@ -674,7 +965,8 @@ flce_status flce_forward_backward(const flce_problem* p, const void* H, const vo
   if (!aligned(dW, 16) || !aligned(dH, 16)) return FLCE_ERR_UNSUPPORTED;
   int sms = 0;
   if (!device_setup(&sms)) return FLCE_ERR_CUDA;
-  const Plan pl = make_plan(*p);
+  Plan pl = make_plan(*p);
+  choose_backward_chunk(pl, *p, sms);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float* lse_buf = lse ? lse : reinterpret_cast<float*>(wsb + pl.off_lse);
@@ -690,7 +982,61 @@ flce_status flce_forward_backward(const flce_problem* p, const void* H, const vo
   if (!build_maps(*p, pl, H, W, dH, dW, wsb, true, &mp)) return FLCE_ERR_CUDA;
   flce_status r = run_forward(*p, pl, mp, y, lse_buf, loss, grad_loss, wsb, sms, st);
   if (r != FLCE_OK) return r;
-  return run_backward(*p, pl, mp, y, lse_buf, wsb, sms, st);
+  return run_backward_any(*p, pl, mp, H, W, y, lse_buf, dH, dW, wsb, sms, st, nullptr, nullptr, nullptr);
+}
+
+flce_status flce_forward_ex(const flce_problem* p, int32_t reduction, const void* H, const void* W, const float* bias,
+                            const int64_t* y, float* lse, float* loss, void* ws, size_t ws_bytes, void* stream) {
+  flce_status s = check_common(p, H, W, y, loss, ws, ws_bytes);
+  if (s != FLCE_OK) return s;
+  if (reduction < FLCE_REDUCTION_MEAN || reduction > FLCE_REDUCTION_NONE) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->n_rows > 0 && !lse) return FLCE_ERR_INVALID_ARGUMENT;
+  int sms = 0;
+  if (!device_setup(&sms)) return FLCE_ERR_CUDA;
+  const Plan pl = make_plan(*p);
+  Maps mp;
+  if (p->n_rows > 0 && !build_maps(*p, pl, H, W, nullptr, nullptr, static_cast<uint8_t*>(ws), false, &mp))
+    return FLCE_ERR_CUDA;
+  return run_forward(*p, pl, mp, y, lse, loss, 1.0f, static_cast<uint8_t*>(ws), sms,
+                     static_cast<cudaStream_t>(stream), bias, reduction,
+                     reduction == FLCE_REDUCTION_NONE ? loss : nullptr);
+}
+
+flce_status flce_backward_ex(const flce_problem* p, int32_t reduction, const void* H, const void* W,
+                             const float* bias, const int64_t* y, const float* lse, const float* grad, float* dH,
+                             float* dW, float* dbias, void* ws, size_t ws_bytes, void* stream) {
+  if (!grad) return FLCE_ERR_INVALID_ARGUMENT;
+  flce_status s = check_common(p, H, W, y, grad, ws, ws_bytes);
+  if (s != FLCE_OK) return s;
+  if (reduction < FLCE_REDUCTION_MEAN || reduction > FLCE_REDUCTION_NONE) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!dW || (p->n_rows > 0 && (!dH || !lse))) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(dW, 16) || !aligned(dH, 16)) return FLCE_ERR_UNSUPPORTED;
+  int sms = 0;
+  if (!device_setup(&sms)) return FLCE_ERR_CUDA;
+  Plan pl = make_plan(*p);
+  choose_backward_chunk(pl, *p, sms);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(wsb);
+  {
+    ProfScope prof(FLCE_KERNEL_PREP, st);
+    prep_kernel<<<1, 1024, 0, st>>>(y, p->n_rows, p->vocab, p->ignore_index, p->filter_eps > 0.f ? 1u : 0u, hdr);
+    if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+  {
+    ProfScope prof(FLCE_KERNEL_SET_SCALE, st);
+    set_scale_kernel<<<1, 32, 0, st>>>(grad, reduction, hdr);
+    if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+  if (p->n_rows == 0) {
+    if (cudaMemsetAsync(dW, 0, (size_t)p->vocab * p->hidden * 4, st) != cudaSuccess) return FLCE_ERR_CUDA;
+    if (dbias && cudaMemsetAsync(dbias, 0, (size_t)p->vocab * 4, st) != cudaSuccess) return FLCE_ERR_CUDA;
+    return FLCE_OK;
+  }
+  Maps mp;
+  if (!build_maps(*p, pl, H, W, dH, dW, wsb, true, &mp)) return FLCE_ERR_CUDA;
+  return run_backward_any(*p, pl, mp, H, W, y, lse, dH, dW, wsb, sms, st, bias,
+                          reduction == FLCE_REDUCTION_NONE ? grad : nullptr, dbias);
 }
 
 flce_status flce_get_device_status(void* ws, void* stream) {

@@ -79,6 +79,8 @@ struct GemmParams {
   int64_t ignore_index;
   const int64_t* y;
   const float* lse;            // DZ: natural-log LSE per global row
+  const float* bias;           // LSE / DZ: optional fp32 bias per vocabulary id (logit = h.w + b)
+  const float* row_scale;      // DZ: optional per-global-row factor applied to G before rounding
   float* part_m;               // LSE: running max (log2 units) [tiles][part_ld]
   float* part_s;               // LSE: sum of 2^(t - max)       [tiles][part_ld]
   float* zy;                   // LSE: target logit per local row
@@ -158,6 +160,222 @@ __device__ __forceinline__ bool kblock_skipped_group(const GemmParams& p, int mt
 __device__ __forceinline__ void record_timeout(uint32_t* status, volatile uint32_t* abort_flag) {
   *abort_flag = 1u;
   atomicOr(status, kDevTimeout);
+}
+
+// Epilogue of one accumulator tile, run by the four epilogue warps with one
+// tile row per thread (TMEM lane quarter q, lane `lane`). Each warp reports
+// through `rel`, once it has read the whole accumulator, that the TMEM buffer
+// may be reused; `ebuf` is the warp's staging-box toggle.
+struct AccRelease {
+  uint64_t* local;          // barrier in this CTA, or
+  uint32_t cluster_addr;    // its shared::cluster address in the MMA-issuing CTA
+  bool remote;
+  __device__ __forceinline__ void arrive() const {
+    if (remote)
+      ptx::mbar_arrive_cluster(cluster_addr);
+    else
+      ptx::mbar_arrive(local);
+  }
+};
+
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtensorMap* tmOut, int mt, int nt,
+                                              uint32_t taddr, int q, int lane, uint8_t* my_boxes, uint32_t& ebuf,
+                                              const AccRelease& rel) {
+  const int r_local = q * 32 + lane;
+  const int lrow = mt * kBM + r_local;         // local row of this launch
+  if (mt >= p.m_tiles) {
+    // The empty half of a cluster's last group: nothing to write.
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) rel.arrive();
+  } else if (p.mode == EPI_LSE) {
+    const bool in_rows = lrow < p.m_valid && (p.row0 + lrow) < p.n_rows;
+    const int grow = p.row0 + lrow;
+    const int col_t0 = p.col0 + nt * kBN;
+    int yl = -1;
+    if (in_rows) {
+      const int64_t yv = __ldg(p.y + grow);
+      if (yv != p.ignore_index && yv >= 0 && yv < p.n_cols) yl = (int)(yv - col_t0);
+    }
+    const bool ragged = col_t0 + kBN > p.n_cols;
+    float run_max = -INFINITY, run_sum = 0.f, zt = 0.f;
+    bool has_t = false;
+#pragma unroll 1
+    for (int c = 0; c < kBN; c += 32) {
+      uint32_t r[32];
+      ptx::tmem_ld_32x32b_x32(taddr + c, r);
+      ptx::tmem_ld_wait();
+      float x[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
+      if (p.bias) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col_t0 + c + j < p.n_cols) x[j] += __ldg(p.bias + col_t0 + c + j);
+      }
+      if (ragged) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (col_t0 + c + j >= p.n_cols) x[j] = -INFINITY;
+      }
+      if ((unsigned)(yl - c) < 32u) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j == yl - c) zt = x[j];
+        has_t = true;
+      }
+      float cmax = x[0];
+#pragma unroll
+      for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, x[j]);
+      const float new_max = fmaxf(run_max, cmax * kLog2e);
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc += ptx::ex2_approx(fmaf(x[j], kLog2e, -new_max));
+      run_sum = run_sum * ptx::ex2_approx(run_max - new_max) + acc;
+      run_max = new_max;
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) rel.arrive();
+    if (in_rows) {
+      const size_t idx = (size_t)(p.part_t0 + nt) * p.part_ld + lrow;
+      p.part_m[idx] = run_max;
+      p.part_s[idx] = run_sum;
+      if (has_t) p.zy[lrow] = zt;
+    }
+  } else if (p.mode == EPI_DZ) {
+    const int grow = p.row0 + lrow;
+    const bool in_rows = lrow < p.m_valid && grow < p.n_rows;
+    const int col_t0 = p.col0 + nt * kBN;
+    bool valid = false;
+    int yl = -1;
+    float lse2 = 0.f, rs = 1.f;
+    if (in_rows) {
+      const int64_t yv = __ldg(p.y + grow);
+      valid = yv != p.ignore_index && yv >= 0 && yv < p.n_cols;
+      if (valid) {
+        yl = (int)(yv - col_t0);
+        lse2 = __ldg(p.lse + grow) * kLog2e;
+        if (p.row_scale) rs = __ldg(p.row_scale + grow);
+      }
+    }
+    const bool ragged = col_t0 + kBN > p.n_cols;
+    float amax = 0.f;
+#pragma unroll 1
+    for (int box = 0; box < kBN / 64; ++box) {
+      uint8_t* sbox = my_boxes + ebuf * kEpiBoxBytes;
+      if (lane == 0) ptx::bulk_wait_group_read<1>();
+      __syncwarp();
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int c = box * 64 + half * 32;
+        uint32_t r[32];
+        ptx::tmem_ld_32x32b_x32(taddr + c, r);
+        ptx::tmem_ld_wait();
+        float g[32];
+        if (p.bias) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (col_t0 + c + j < p.n_cols) r[j] = __float_as_uint(__uint_as_float(r[j]) + __ldg(p.bias + col_t0 + c + j));
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          g[j] = valid ? ptx::ex2_approx(fmaf(__uint_as_float(r[j]), kLog2e, -lse2)) : 0.f;
+        if (ragged) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (col_t0 + c + j >= p.n_cols) g[j] = 0.f;
+        }
+        if ((unsigned)(yl - c) < 32u) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == yl - c) g[j] -= 1.f;
+        }
+        if (p.filter) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(g[j]));
+        }
+        if (p.row_scale) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) g[j] *= rs;
+        }
+        uint32_t packed[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(g[2 * j], g[2 * j + 1]);
+          packed[j] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int chunk = (half * 4 + v) ^ (lane & 7);
+          uint4 val = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+          *reinterpret_cast<uint4*>(sbox + lane * 128 + chunk * 16) = val;
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_2d(tmOut, sbox, nt * kBN + box * 64, mt * kBM + q * 32);
+        ptx::bulk_commit_group();
+      }
+      ebuf ^= 1u;
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) rel.arrive();
+    if (p.filter) {
+      // Staging tile (mt, nt) gets one byte per 32-row quarter; the tile
+      // is skipped downstream when the whole 32-bit word is zero.
+      const unsigned keep = __any_sync(0xffffffffu, amax >= p.filter_eps) ? 1u : 0u;
+      if (lane == 0) reinterpret_cast<uint8_t*>(p.flags + (size_t)mt * p.flags_ld + nt)[q] = (uint8_t)keep;
+    }
+  } else {
+    // EPI_STORE / EPI_REDUCE
+    bool all_skipped = p.skip_by_flags != 0;
+    if (p.skip_by_flags) {
+      for (int kb = 0; kb < p.k_blocks && all_skipped; ++kb) all_skipped = kblock_skipped(p, mt, kb);
+    }
+    const float sc = __ldg(p.scale);
+    if (!(all_skipped && p.mode == EPI_REDUCE)) {
+#pragma unroll 1
+      for (int c = 0; c < kBN; c += 32) {
+        uint8_t* sbox = my_boxes + ebuf * kEpiBoxBytes;
+        if (lane == 0) ptx::bulk_wait_group_read<1>();
+        __syncwarp();
+        float x[32];
+        if (all_skipped) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = 0.f;
+        } else {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c, r);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * sc;
+        }
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const int chunk = v ^ (lane & 7);
+          *reinterpret_cast<float4*>(sbox + lane * 128 + chunk * 16) =
+              make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int32_t c0 = nt * kBN + c, c1 = p.out_m0 + mt * kBM + q * 32;
+          if (p.mode == EPI_REDUCE)
+            ptx::tma_reduce_add_2d(tmOut, sbox, c0, c1);
+          else
+            ptx::tma_store_2d(tmOut, sbox, c0, c1);
+          ptx::bulk_commit_group();
+        }
+        ebuf ^= 1u;
+      }
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) rel.arrive();
+  }
 }
 
 // kCluster = 1: every CTA loads its own A and B tiles.
@@ -352,7 +570,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                    // TMEM lane quarter this warp may read
-    const int r_local = q * 32 + lane;         // row of the tile owned by this thread
     uint8_t* my_boxes = epi_smem + q * 2 * kEpiBoxBytes;
     uint32_t ebuf = 0;
     int i = 0;
@@ -369,186 +586,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
       }
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + buf * kBN + ((uint32_t)(q * 32) << 16);
-      const int lrow = mt * kBM + r_local;     // local row of this launch
 
-      if (mt >= p.m_tiles) {
-        // The empty half of a cluster's last group: nothing to write.
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
-      } else if (p.mode == EPI_LSE) {
-        const bool in_rows = lrow < p.m_valid && (p.row0 + lrow) < p.n_rows;
-        const int grow = p.row0 + lrow;
-        const int col_t0 = p.col0 + nt * kBN;
-        int yl = -1;
-        if (in_rows) {
-          const int64_t yv = __ldg(p.y + grow);
-          if (yv != p.ignore_index && yv >= 0 && yv < p.n_cols) yl = (int)(yv - col_t0);
-        }
-        const bool ragged = col_t0 + kBN > p.n_cols;
-        float run_max = -INFINITY, run_sum = 0.f, zt = 0.f;
-        bool has_t = false;
-#pragma unroll 1
-        for (int c = 0; c < kBN; c += 32) {
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c, r);
-          ptx::tmem_ld_wait();
-          float x[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]);
-          if (ragged) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (col_t0 + c + j >= p.n_cols) x[j] = -INFINITY;
-          }
-          if ((unsigned)(yl - c) < 32u) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j == yl - c) zt = x[j];
-            has_t = true;
-          }
-          float cmax = x[0];
-#pragma unroll
-          for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, x[j]);
-          const float new_max = fmaxf(run_max, cmax * kLog2e);
-          float acc = 0.f;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) acc += ptx::ex2_approx(fmaf(x[j], kLog2e, -new_max));
-          run_sum = run_sum * ptx::ex2_approx(run_max - new_max) + acc;
-          run_max = new_max;
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
-        if (in_rows) {
-          const size_t idx = (size_t)(p.part_t0 + nt) * p.part_ld + lrow;
-          p.part_m[idx] = run_max;
-          p.part_s[idx] = run_sum;
-          if (has_t) p.zy[lrow] = zt;
-        }
-      } else if (p.mode == EPI_DZ) {
-        const int grow = p.row0 + lrow;
-        const bool in_rows = lrow < p.m_valid && grow < p.n_rows;
-        const int col_t0 = p.col0 + nt * kBN;
-        bool valid = false;
-        int yl = -1;
-        float lse2 = 0.f;
-        if (in_rows) {
-          const int64_t yv = __ldg(p.y + grow);
-          valid = yv != p.ignore_index && yv >= 0 && yv < p.n_cols;
-          if (valid) {
-            yl = (int)(yv - col_t0);
-            lse2 = __ldg(p.lse + grow) * kLog2e;
-          }
-        }
-        const bool ragged = col_t0 + kBN > p.n_cols;
-        float amax = 0.f;
-#pragma unroll 1
-        for (int box = 0; box < kBN / 64; ++box) {
-          uint8_t* sbox = my_boxes + ebuf * kEpiBoxBytes;
-          if (lane == 0) ptx::bulk_wait_group_read<1>();
-          __syncwarp();
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int c = box * 64 + half * 32;
-            uint32_t r[32];
-            ptx::tmem_ld_32x32b_x32(taddr + c, r);
-            ptx::tmem_ld_wait();
-            float g[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              g[j] = valid ? ptx::ex2_approx(fmaf(__uint_as_float(r[j]), kLog2e, -lse2)) : 0.f;
-            if (ragged) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (col_t0 + c + j >= p.n_cols) g[j] = 0.f;
-            }
-            if ((unsigned)(yl - c) < 32u) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j == yl - c) g[j] -= 1.f;
-            }
-            if (p.filter) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(g[j]));
-            }
-            uint32_t packed[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(g[2 * j], g[2 * j + 1]);
-              packed[j] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const int chunk = (half * 4 + v) ^ (lane & 7);
-              uint4 val = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-              *reinterpret_cast<uint4*>(sbox + lane * 128 + chunk * 16) = val;
-            }
-          }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            ptx::tma_store_2d(tmOut, sbox, nt * kBN + box * 64, mt * kBM + q * 32);
-            ptx::bulk_commit_group();
-          }
-          ebuf ^= 1u;
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
-        if (p.filter) {
-          // Staging tile (mt, nt) gets one byte per 32-row quarter; the tile
-          // is skipped downstream when the whole 32-bit word is zero.
-          const unsigned keep = __any_sync(0xffffffffu, amax >= p.filter_eps) ? 1u : 0u;
-          if (lane == 0) reinterpret_cast<uint8_t*>(p.flags + (size_t)mt * p.flags_ld + nt)[q] = (uint8_t)keep;
-        }
-      } else {
-        // EPI_STORE / EPI_REDUCE
-        bool all_skipped = p.skip_by_flags != 0;
-        if (p.skip_by_flags) {
-          for (int kb = 0; kb < p.k_blocks && all_skipped; ++kb) all_skipped = kblock_skipped(p, mt, kb);
-        }
-        const float sc = __ldg(p.scale);
-        if (!(all_skipped && p.mode == EPI_REDUCE)) {
-#pragma unroll 1
-          for (int c = 0; c < kBN; c += 32) {
-            uint8_t* sbox = my_boxes + ebuf * kEpiBoxBytes;
-            if (lane == 0) ptx::bulk_wait_group_read<1>();
-            __syncwarp();
-            float x[32];
-            if (all_skipped) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) x[j] = 0.f;
-            } else {
-              uint32_t r[32];
-              ptx::tmem_ld_32x32b_x32(taddr + c, r);
-              ptx::tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * sc;
-            }
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const int chunk = v ^ (lane & 7);
-              *reinterpret_cast<float4*>(sbox + lane * 128 + chunk * 16) =
-                  make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
-            }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              const int32_t c0 = nt * kBN + c, c1 = p.out_m0 + mt * kBM + q * 32;
-              if (p.mode == EPI_REDUCE)
-                ptx::tma_reduce_add_2d(tmOut, sbox, c0, c1);
-              else
-                ptx::tma_store_2d(tmOut, sbox, c0, c1);
-              ptx::bulk_commit_group();
-            }
-            ebuf ^= 1u;
-          }
-        }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&acc_empty[buf]);
-      }
+      const AccRelease rel{&acc_empty[buf], 0u, false};
+      epilogue_tile(p, tmOut, mt, nt, taddr, q, lane, my_boxes, ebuf, rel);
     }
     if (lane == 0) ptx::bulk_wait_group<0>();
     __syncwarp();

@@ -1,0 +1,224 @@
+// The GEMM of tile_gemm.cuh on CTA pairs: tcgen05.mma.cta_group::2 with
+// M = 256 (128 rows in each CTA of a 2-CTA cluster) and N = 256.
+//
+// Each CTA streams its own 128x64 A box and its half (128 of the 256
+// columns) of the B tile into a 6-stage ring; the pair's tensor cores share
+// the two B halves, so every SM moves 32 KiB per 64-deep k-block instead of
+// 48 KiB, and more stages fit in shared memory. The even CTA's producer
+// expects the bytes of both CTAs on its full barrier, the odd CTA's TMA
+// loads complete on that barrier, and the even CTA's single MMA thread
+// issues the MMAs and releases both CTAs' stages and accumulators with
+// multicast commits. Each CTA's epilogue warps read their own 128 TMEM lanes
+// and report to the even CTA that the accumulator buffer may be reused.
+//
+// Used for launches without gradient filtering (the pair computes both
+// halves of a group, so it cannot leave out one half's k-blocks).
+#pragma once
+
+#include "tile_gemm.cuh"
+
+namespace flce {
+
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairBBytes = (kBN / 2) * kBK * 2;           // 16 KiB: this CTA's half of B
+constexpr uint32_t kPairStageBytes = kABytes + kPairBBytes;      // 32 KiB
+constexpr uint32_t kPairSmemBytes = 1024 + kPairStages * kPairStageBytes + kEpiBytes + kBarrierBytes;
+static_assert(kPairSmemBytes <= 232448, "shared memory of the pair kernel");
+
+__global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const __grid_constant__ GemmLaunch L) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* epi_smem = smem + kPairStages * kPairStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + kEpiBytes);
+  uint64_t* full_bar = bars;                        // [kPairStages] (used in the even CTA)
+  uint64_t* empty_bar = bars + kPairStages;         // [kPairStages]
+  uint64_t* acc_full = bars + 2 * kPairStages;      // [2]
+  uint64_t* acc_empty = bars + 2 * kPairStages + 2; // [2] (used in the even CTA)
+  uint64_t* drain_bar = bars + 2 * kPairStages + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 5);
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = L.tile_end[L.n_probs - 1];
+  const uint64_t wait_limit_ns = L.prob[0].wait_limit_ns;
+  uint32_t* const status = L.prob[0].status;
+  const int rank = (int)ptx::cluster_ctarank();
+  const bool leader = rank == 0;
+  const int unit0 = blockIdx.x / 2;
+  const int unit_stride = gridDim.x / 2;
+  constexpr uint16_t kBoth = 3;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(&acc_full[b], 1);
+      ptx::mbar_init(&acc_empty[b], 8);           // 4 epilogue warps in each CTA
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    ptx::fence_mbarrier_init();
+    for (int q = 0; q < L.n_probs; ++q) {
+      ptx::prefetch_tmap(&L.tm_a[q]);
+      ptx::prefetch_tmap(&L.tm_b[q]);
+      ptx::prefetch_tmap(&L.tm_out[q]);
+    }
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(tmem_slot, kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync_all();                          // both CTAs' barriers exist
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      const uint32_t full_leader = ptx::map_to_rank(&full_bar[0], 0);
+      uint32_t stage = 0, phase = 0;
+      int32_t last_parity[kPairStages];
+      for (int s = 0; s < kPairStages; ++s) last_parity[s] = -1;
+      bool ok = true;
+      for (int t = unit0; t < num_tiles && ok; t += unit_stride) {
+        int pi, mt, nt;
+        const int tl = decode_tile(L, t, pi);
+        const GemmParams& p = L.prob[pi];
+        const CUtensorMap* tmA = &L.tm_a[pi];
+        const CUtensorMap* tmB = &L.tm_b[pi];
+        tile_coords(p, tl, 2, rank, mt, nt);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, wait_limit_ns, abort_flag)) {
+            record_timeout(status, abort_flag);
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * kPairStageBytes;
+          uint8_t* sb = sa + kABytes;
+          const uint32_t fb = full_leader + stage * 8u;
+          if (leader) ptx::mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
+          const int32_t kc = kb * kBK;
+          if (p.a_mn) {
+            for (int h = 0; h < kBM / 64; ++h)
+              ptx::tma_load_2d_pair(sa + h * 8192, tmA, p.a_m0 + mt * kBM + h * 64, p.a_k0 + kc, fb);
+          } else {
+            ptx::tma_load_2d_pair(sa, tmA, p.a_k0 + kc, p.a_m0 + mt * kBM, fb);
+          }
+          const int32_t n_half = p.b_n0 + nt * kBN + rank * (kBN / 2);
+          if (p.b_mn) {
+            for (int h = 0; h < (kBN / 2) / 64; ++h)
+              ptx::tma_load_2d_pair(sb + h * 8192, tmB, n_half + h * 64, p.b_k0 + kc, fb);
+          } else {
+            ptx::tma_load_2d_pair(sb, tmB, p.b_k0 + kc, n_half, fb);
+          }
+          last_parity[stage] = (int32_t)phase;
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        // The even CTA's full barriers count both CTAs' bytes: once a phase
+        // completes, no copy of that phase is still landing in either CTA.
+        volatile uint32_t never = 0u;
+        for (int s = 0; s < kPairStages; ++s)
+          if (last_parity[s] >= 0) ptx::mbar_wait_bounded(&full_bar[s], (uint32_t)last_parity[s], 100000000ull, &never);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (lane == 0 && leader) {
+      const uint32_t smem_base = ptx::smem_u32(smem);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      int i = 0;
+      for (int t = unit0; t < num_tiles && ok; t += unit_stride, ++i) {
+        int pi, mt, nt;
+        const int tl = decode_tile(L, t, pi);
+        const GemmParams& p = L.prob[pi];
+        tile_coords(p, tl, 2, rank, mt, nt);
+        const uint32_t idesc = ptx::idesc_bf16_f32(2 * kBM, kBN, p.a_mn != 0, p.b_mn != 0);
+        const uint32_t buf = i & 1, use = i >> 1;
+        if (!ptx::mbar_wait_bounded(&acc_empty[buf], (use & 1u) ^ 1u, wait_limit_ns, abort_flag)) {
+          record_timeout(status, abort_flag);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + buf * kBN;
+        uint32_t accumulate = 0;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!ptx::mbar_wait_bounded(&full_bar[stage], phase, wait_limit_ns, abort_flag)) {
+            record_timeout(status, abort_flag);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = smem_base + stage * kPairStageBytes;
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t adesc = p.a_mn ? ptx::smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                          : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
+            const uint64_t bdesc = p.b_mn ? ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                          : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
+            ptx::mma_bf16_ss_pair(d_tmem, adesc, bdesc, idesc, accumulate);
+            accumulate = 1;
+          }
+          ptx::mma_commit_pair_multicast(&empty_bar[stage], kBoth);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair_multicast(&acc_full[buf], kBoth);
+      }
+      // Every MMA issued has completed once the drain barrier flips.
+      ptx::mma_commit_pair_multicast(drain_bar, 1);
+      volatile uint32_t never = 0u;
+      ptx::mbar_wait_bounded(drain_bar, 0u, 100000000ull, &never);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    uint8_t* my_boxes = epi_smem + q * 2 * kEpiBoxBytes;
+    uint32_t ebuf = 0;
+    int i = 0;
+    for (int t = unit0; t < num_tiles; t += unit_stride, ++i) {
+      int pi, mt, nt;
+      const int tl = decode_tile(L, t, pi);
+      const GemmParams& p = L.prob[pi];
+      const CUtensorMap* tmOut = &L.tm_out[pi];
+      tile_coords(p, tl, 2, rank, mt, nt);
+      const uint32_t buf = i & 1, use = i >> 1;
+      if (!ptx::mbar_wait_bounded(&acc_full[buf], use & 1u, wait_limit_ns, abort_flag)) {
+        record_timeout(status, abort_flag);
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem_base + buf * kBN + ((uint32_t)(q * 32) << 16);
+      const AccRelease rel{&acc_empty[buf], ptx::map_to_rank(&acc_empty[buf], 0), !leader};
+      epilogue_tile(p, tmOut, mt, nt, taddr, q, lane, my_boxes, ebuf, rel);
+    }
+    if (lane == 0) ptx::bulk_wait_group<0>();
+    __syncwarp();
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync_all();                          // the pair is done with both CTAs' TMEM and smem
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
+}  // namespace flce

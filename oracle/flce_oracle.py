@@ -180,13 +180,16 @@ def dW_rows(H, W, y, lse, vocab_ids, grad_loss: float = 1.0, ignore_index: int =
 
 
 def forward_backward_filtered(H, W, y, eps: float, tile_rows: int, tile_cols: int,
-                              grad_loss: float = 1.0, ignore_index: int = IGNORE_INDEX):
+                              grad_loss: float = 1.0, ignore_index: int = IGNORE_INDEX,
+                              filter_dH: bool = True, filter_dW: bool = True):
     """Gradient filtering of Cut Cross-Entropy Alg. 4, emulated in fp64.
 
     The dZ matrix is cut into tile_rows x tile_cols tiles aligned at 0; a tile
     whose unscaled gradient G = softmax - onehot has every |G| < eps (ignored
-    rows count as G = 0) contributes nothing to dH or dW. Returns the same
-    tuple as forward_backward plus the fraction of tiles skipped.
+    rows count as G = 0) contributes nothing to dH or dW. filter_dH /
+    filter_dW = False computes that gradient from the full G (the paper's
+    CCE-FullE / CCE-FullC variants). Returns the same tuple as
+    forward_backward plus the fraction of tiles skipped.
     """
     n, vocab = H.shape[0], W.shape[0]
     y = _check_targets(y, vocab, ignore_index)
@@ -200,15 +203,15 @@ def forward_backward_filtered(H, W, y, eps: float, tile_rows: int, tile_cols: in
         r1 = min(n, r0 + tile_rows)
         z = logits(H[r0:r1], W)
         g = _dlogits_block(z, lse[r0:r1], y[r0:r1], 1.0, ignore_index)
+        g_full = g.copy()
         for c0 in range(0, vocab, tile_cols):
             c1 = min(vocab, c0 + tile_cols)
             tiles += 1
             if np.all(np.abs(g[:, c0:c1]) < eps):
                 skipped += 1
                 g[:, c0:c1] = 0.0
-        dz = g * scale
-        dH[r0:r1] = dz @ W
-        dW += dz.T @ H[r0:r1]
+        dH[r0:r1] = ((g if filter_dH else g_full) * scale) @ W
+        dW += ((g if filter_dW else g_full) * scale).T @ H[r0:r1]
     return lse, loss, dH, dW, count, skipped / max(tiles, 1)
 
 

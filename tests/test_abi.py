@@ -19,7 +19,8 @@ def test_library_exports_every_declared_symbol():
     declared = flce.declared_symbols()
     assert set(declared) == {"flce_workspace_bytes", "flce_forward", "flce_forward_backward",
                              "flce_get_device_status", "flce_status_string", "flce_get_filter_stats",
-                             "flce_profile_set", "flce_profile_count", "flce_forward_static_scratch"}
+                             "flce_profile_set", "flce_profile_count", "flce_forward_static_scratch",
+                             "flce_forward_ex", "flce_backward_ex"}
     out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
     for name in declared:
@@ -45,6 +46,12 @@ def test_workspace_is_linear_in_rows_and_vocab_never_n_times_v():
     assert ws_long < 131072 * 151552 * 2 / 100
     # Tiny problems need little.
     assert flce.flce_workspace_bytes(flce.make_problem(1, 8, 1)) < 1 << 20
+
+
+def test_compaction_workspace_is_linear_in_rows():
+    base = flce.flce_workspace_bytes(flce.make_problem(8192, 2048, 151552))
+    comp = flce.flce_workspace_bytes(flce.make_problem(8192, 2048, 151552, flags=flce.FLAG_COMPACT_IGNORED))
+    assert 0 < comp - base <= 8192 * 2048 * 6 + 8192 * 28 + 8 * 1024
 
 
 def test_workspace_bytes_rejects_bad_problems():
@@ -81,13 +88,28 @@ def test_host_argument_checks_return_before_any_launch():
     assert _fwd(good, H=FAKE + 8) == Status.ERR_UNSUPPORTED                 # TMA needs 16-byte alignment
     assert _fwd(good, nb=flce.flce_workspace_bytes(good) - 1) == Status.ERR_WORKSPACE_TOO_SMALL
     assert _fwd(flce.make_problem(16, 60, 100)) == Status.ERR_UNSUPPORTED   # D % 8 != 0
-    assert _fwd(flce.make_problem(16, 64, 100, flags=0x4)) == Status.ERR_INVALID_ARGUMENT
+    assert _fwd(flce.make_problem(16, 64, 100, flags=0x10)) == Status.ERR_INVALID_ARGUMENT
     assert _fwd(flce.make_problem(16, 64, 100, filter_eps=float("nan"))) == Status.ERR_INVALID_ARGUMENT
     assert _fb(good, dW=None) == Status.ERR_INVALID_ARGUMENT
     assert _fb(good, dH=None) == Status.ERR_INVALID_ARGUMENT
     assert _fb(good, dH=FAKE + 4) == Status.ERR_UNSUPPORTED
     assert _fb(good, g=float("inf")) == Status.ERR_INVALID_ARGUMENT
     assert _fb(good, nb=1) == Status.ERR_WORKSPACE_TOO_SMALL
+
+
+def test_general_entry_points_check_arguments():
+    good = flce.make_problem(16, 64, 100)
+    nb = flce.flce_workspace_bytes(good)
+    assert flce.flce_forward_ex(good, 3, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, nb, 0) == Status.ERR_INVALID_ARGUMENT
+    assert flce.flce_forward_ex(good, 2, FAKE, FAKE, None, FAKE, None, FAKE, FAKE, nb, 0) == Status.ERR_INVALID_ARGUMENT
+    assert flce.flce_backward_ex(good, 0, FAKE, FAKE, None, FAKE, FAKE, None, FAKE, FAKE, None, FAKE, nb,
+                                 0) == Status.ERR_INVALID_ARGUMENT
+    assert flce.flce_backward_ex(good, 0, FAKE, FAKE, None, FAKE, None, FAKE, FAKE, FAKE, None, FAKE, nb,
+                                 0) == Status.ERR_INVALID_ARGUMENT
+    assert flce.flce_backward_ex(good, 0, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE + 4, None, FAKE, nb,
+                                 0) == Status.ERR_UNSUPPORTED
+    assert flce.flce_backward_ex(good, 9, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, nb,
+                                 0) == Status.ERR_INVALID_ARGUMENT
 
 
 def test_profile_hook_arguments():

@@ -279,3 +279,13 @@ def test_general_form_reduces_to_the_plain_mean():
     lse, loss, dH, dW, _ = oracle.forward_backward(H, W, y, grad_loss=2.0)
     assert abs(a["loss"] - loss) < 1e-14
     assert np.max(np.abs(a["dH"] - dH)) < 1e-15 and np.max(np.abs(a["dW"] - dW)) < 1e-15
+
+
+def test_filter_full_variants():
+    H, W, y = _rand(34, 24, 6, 64, w_scale=2.0, ignore=(3,))
+    full = oracle.forward_backward(H, W, y)
+    f = oracle.forward_backward_filtered(H, W, y, 1e-3, 8, 16)
+    fc = oracle.forward_backward_filtered(H, W, y, 1e-3, 8, 16, filter_dW=False)
+    fe = oracle.forward_backward_filtered(H, W, y, 1e-3, 8, 16, filter_dH=False)
+    assert np.array_equal(fc[2], f[2]) and np.max(np.abs(fc[3] - full[3])) < 1e-15
+    assert np.array_equal(fe[3], f[3]) and np.max(np.abs(fe[2] - full[2])) < 1e-15
