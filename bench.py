@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gravity16b_head", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--filter-eps", type=float, default=0.0)
+    ap.add_argument("--compact-ignored", action="store_true",
+                    help="remove ignored rows before the backward (FLCE_FLAG_COMPACT_IGNORED)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -80,6 +82,33 @@ def weak_scaling_throughput(rows_per_rank: int, world: int, steps: int, max_tota
 def rank_seed(base_seed: int, rank: int) -> int:
     """Each rank draws its own batch (independent problems, weak scaling)."""
     return base_seed + rank
+
+
+def kernel_sources_sha256() -> str:
+    """Digest of the CUDA sources: a recorded DRAM capture is only used while it matches."""
+    import hashlib
+    csrc = os.path.join(ROOT, "lm_head_loss_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per GEMM launch from the committed ncu capture of this
+    workload, or None when there is none or the kernels changed since."""
+    path = os.path.join(ROOT, "profiles", "gemm_dram_traffic.json")
+    if not os.path.exists(path):
+        return None, "no DRAM capture recorded"
+    with open(path) as f:
+        rec = json.load(f)
+    if rec.get("workload") != workload:
+        return None, "DRAM capture recorded for another workload"
+    if rec.get("kernel_sources_sha256") != kernel_sources_sha256():
+        return None, "kernel sources changed since the DRAM capture"
+    return float(rec["dram_bytes_per_gemm_launch"]) / 1e9, rec.get("command", "")
 
 
 def measured_peaks():
@@ -194,7 +223,8 @@ def run_ours(args, rank, world, local):
     H = torch.from_numpy(inp["H"].view(np.int16)).view(torch.bfloat16).to(dev)
     W = torch.from_numpy(inp["W"].view(np.int16)).view(torch.bfloat16).to(dev)
     y = torch.from_numpy(inp["y"]).to(dev)
-    prob = flce.make_problem(N, D, V, -100, args.filter_eps, 0)
+    prob = flce.make_problem(N, D, V, -100, args.filter_eps,
+                             flce.FLAG_COMPACT_IGNORED if args.compact_ignored else 0)
     ws_bytes = flce.flce_workspace_bytes(prob)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     loss = torch.empty((), dtype=torch.float32, device=dev)
@@ -253,6 +283,7 @@ def run_ours(args, rank, world, local):
 
     flops_step = 8.0 * N * V * D
     peaks, peak_src = measured_peaks()
+    traffic_gb, traffic_note = recorded_traffic(wl.name)
     gemm_ms = sum(v["ms"] for k, v in per_kind.items() if k.startswith("gemm_"))
     gemm_launches = sum(v["launches"] for k, v in per_kind.items() if k.startswith("gemm_"))
     achieved = flops_step * args.steps / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
@@ -265,13 +296,16 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "n_rows": N, "hidden": D, "vocab": V, "global_batch_rows": N * world,
                    "targets": wl.targets, "ignore_frac": wl.ignore_frac, "filter_eps": args.filter_eps,
+                   "compact_ignored": bool(args.compact_ignored),
                    "parallelism": f"dp{world} (independent batches, no collective)",
                    "l2": "no flush: W (592 MiB bf16) alone exceeds the 129 MB L2 every step"},
         "tflops": step_tflops,
         "pct_bf16_peak": 100.0 * step_tflops / peak,
         "pct_bf16_peak_burst": 100.0 * step_tflops / float(peaks["bf16_tflops"]),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": (achieved / peak) if achieved else None, "traffic": None,
+                     "frac": (achieved / peak) if achieved else None, "traffic": traffic_gb,
+                     "traffic_unit": "GB per launch (dram__bytes_read.sum + dram__bytes_write.sum)",
+                     "traffic_source": traffic_note,
                      "kernel": "flce_gemm_kernel (all four epilogues)",
                      "flops_per_launch": flops_step / (gemm_launches / args.steps) if gemm_launches else None,
                      "launches_per_step": gemm_launches / args.steps if gemm_launches else None,

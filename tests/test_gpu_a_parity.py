@@ -179,3 +179,34 @@ def test_filtered_gradient_matches_tile_mask_oracle():
     assert abs(got["skipped"] - frac) <= 0.02
     assert e_filt["dH_rel"] <= 1e-2 and e_filt["dW_rel"] <= 1e-2
     assert e_full["loss_rel"] <= 1e-3 and e_full["lse_abs"] <= 2e-3
+
+
+def test_cuda_graph_capture_and_replay():
+    # The call allocates nothing and only enqueues work on the given stream, so
+    # it can be captured once and replayed; replays match the eager call bit
+    # for bit (the path is deterministic). The eager call comes first: it sets
+    # up the device (kernel attributes), which is not a stream operation.
+    inp = small_inputs(2000, 256, 9000, seed=77, targets="zipf")
+    H, W, y = to_device(inp)
+    prob = flce.make_problem(2000, 256, 9000)
+    ws = torch.empty(flce.flce_workspace_bytes(prob), dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((), device="cuda"), torch.empty(2000, device="cuda"),
+            torch.empty(2000, 256, device="cuda"), torch.empty(9000, 256, device="cuda")]
+    loss, lse, dH, dW = outs
+    assert flce.flce_forward_backward(prob, H, W, y, 1.0, lse, loss, dH, dW, ws) == flce.Status.OK
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in outs]
+    for t in outs:
+        t.zero_()
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        st = flce.flce_forward_backward(prob, H, W, y, 1.0, lse, loss, dH, dW, ws, stream=side)
+    assert st == flce.Status.OK
+    for _ in range(2):
+        for t in outs:
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(outs, eager):
+            assert torch.equal(a, b)
