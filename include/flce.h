@@ -32,8 +32,9 @@
  *  - ws is a caller-owned device workspace of at least
  *    flce_workspace_bytes(p) bytes, 256-byte aligned. It holds the status
  *    word, per-tile LSE partials, the per-row LSE when the caller passes no
- *    lse buffer, and a bf16 staging buffer for a bounded chunk of dZ. Its size
- *    grows with N + V, never with N * V.
+ *    lse buffer, and two bf16 staging buffers for bounded chunks of dZ
+ *    (at most 8192 x 10240 each). Its size grows with N + V, never with
+ *    N * V.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and the call returns without synchronising. Errors found on the
  *    host are returned before anything is launched. Errors found by the GPU
@@ -72,9 +73,11 @@ typedef struct {
   float filter_eps;      /* gradient filter threshold; 0 = off (default).
                             With eps > 0, a 128-row x 256-column tile of the
                             unscaled gradient softmax - onehot whose entries
-                            are all below eps in magnitude is left out of dH
-                            and dW (Cut Cross-Entropy, Sec. 4.3 "Gradient
-                            filtering" and Alg. 4; the paper uses 2^-12).    */
+                            are all below eps in magnitude is left out of dW,
+                            and a 256-row x 256-column block whose entries
+                            are all below eps is left out of dH (Cut
+                            Cross-Entropy, Sec. 4.3 "Gradient filtering" and
+                            Alg. 4; the paper uses 2^-12).                   */
   uint32_t flags;        /* 0, or FLCE_FLAG_* bits below                   */
 } flce_problem;
 
@@ -100,8 +103,9 @@ typedef struct {
  * grows by about 6*N*D + 28*N bytes. */
 #define FLCE_FLAG_COMPACT_IGNORED 0x8u
 
-/* Bytes of device workspace the two compute calls need for problem *p
- * (0 if p is NULL or invalid). Pure host arithmetic; needs no GPU. */
+/* Bytes of device workspace every compute call below (flce_forward,
+ * flce_forward_backward, flce_forward_ex, flce_backward_ex) needs for
+ * problem *p (0 if p is NULL or invalid). Pure host arithmetic; needs no GPU. */
 size_t flce_workspace_bytes(const flce_problem* p);
 
 /* Forward: per-row LSE (all rows, ignored ones included) and the mean loss.
@@ -160,9 +164,10 @@ flce_status flce_get_device_status(void* ws, void* stream);
 /* Static, human-readable name of a status code. */
 const char* flce_status_string(flce_status s);
 
-/* Statistic of the most recent flce_forward_backward that used `ws` with
- * filtering on: the fraction of 128x256 gradient tiles that were skipped.
- * Synchronises `stream`. Returns 0 when filtering was off. */
+/* Statistic of the most recent backward (flce_forward_backward or
+ * flce_backward_ex) that used `ws` with filtering on: the fraction of 128x256
+ * gradient tiles that were skipped. Synchronises `stream`. Reports 0 when
+ * filtering was off. */
 flce_status flce_get_filter_stats(void* ws, void* stream, double* skipped_fraction);
 
 /* flce_forward without a caller-provided workspace, for callers that cannot
@@ -200,8 +205,8 @@ flce_status flce_forward_static_scratch(const flce_problem* p, const void* H, co
  * it adds two event records per launch on the launch stream. */
 #define FLCE_KERNEL_GEMM_LSE 0
 #define FLCE_KERNEL_GEMM_DZ 1
-#define FLCE_KERNEL_GEMM_DW 2 /* reserved: dW runs inside FLCE_KERNEL_GEMM_BWD launches */
-#define FLCE_KERNEL_GEMM_DH 3 /* reserved: dH runs inside FLCE_KERNEL_GEMM_BWD launches */
+#define FLCE_KERNEL_GEMM_DW 2 /* dW alone (only with FLCE_BWD_GROUPING=0) */
+#define FLCE_KERNEL_GEMM_DH 3 /* dH alone (only with FLCE_BWD_GROUPING=0) */
 #define FLCE_KERNEL_PREP 4
 #define FLCE_KERNEL_COMBINE 5
 #define FLCE_KERNEL_FINALIZE 6

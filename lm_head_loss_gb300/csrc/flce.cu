@@ -516,7 +516,10 @@ static bool device_setup(int* sms_out) {
     if (cudaFuncSetAttribute(flce_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kGemmSmemBytes) != cudaSuccess)
       return false;
-    if (cudaFuncSetAttribute(flce_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(flce_gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kPairSmemBytes) != cudaSuccess)
+      return false;
+    if (cudaFuncSetAttribute(flce_gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kPairSmemBytes) != cudaSuccess)
       return false;
     info[dev].sms = sms;
@@ -532,8 +535,8 @@ static bool device_setup(int* sms_out) {
 //                   tile through TMA multicast;
 //   GEMM_PAIR       2-CTA clusters issuing tcgen05.mma.cta_group::2 (M = 256).
 // GEMM_PAIR is the default; FLCE_GEMM_MODE=cta1|multicast|pair overrides it.
-// Launches that skip filtered k-blocks always use GEMM_CTA1 (the others
-// compute both halves of a group together).
+// With filtering, a 2-CTA variant leaves out a k-block only when both CTAs of
+// the group skip it (coarser dH mask: 256 rows instead of 128).
 enum GemmMode { GEMM_CTA1 = 1, GEMM_MULTICAST = 2, GEMM_PAIR = 3 };
 
 static GemmMode gemm_mode() {
@@ -547,7 +550,18 @@ static GemmMode gemm_mode() {
 }
 
 // Kernel variant of the backward launches, and the vocabulary chunk they use.
-static GemmMode backward_mode(const flce_problem& p) { return p.filter_eps > 0.f ? GEMM_CTA1 : gemm_mode(); }
+static GemmMode backward_mode(const flce_problem&) { return gemm_mode(); }
+
+// The backward groups dW(c), dH(c) and dZ(c+1) into one launch.
+// FLCE_BWD_GROUPING=0 launches them one by one instead (for profiling each
+// contraction on its own; the same work in more launches).
+static bool backward_grouping() {
+  static bool on = [] {
+    const char* e = std::getenv("FLCE_BWD_GROUPING");
+    return !(e && std::strcmp(e, "0") == 0);
+  }();
+  return on;
+}
 
 static void choose_backward_chunk(Plan& pl, const flce_problem& p, int sms) {
   const int cluster = backward_mode(p) == GEMM_CTA1 ? 1 : 2;
@@ -597,7 +611,12 @@ static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (g.mode == GEMM_PAIR) return cudaLaunchKernelEx(&cfg, flce_gemm_pair_kernel, g.L) == cudaSuccess;
+  if (g.mode == GEMM_PAIR) {
+    bool skip = false;
+    for (int q = 0; q < g.L.n_probs; ++q) skip = skip || g.L.prob[q].skip_by_flags != 0;
+    if (skip) return cudaLaunchKernelEx(&cfg, flce_gemm_pair_kernel<true>, g.L) == cudaSuccess;
+    return cudaLaunchKernelEx(&cfg, flce_gemm_pair_kernel<false>, g.L) == cudaSuccess;
+  }
   return cudaLaunchKernelEx(&cfg, flce_gemm_kernel<2>, g.L) == cudaSuccess;
 }
 
@@ -786,11 +805,21 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     g.add(mp.s_k[b], mp.w_mn, mp.dh, dh);
     GemmParams dz_next;
     const bool has_next = s + 1 < items;
-    if (has_next) {
-      dz_next = dz_params(s + 1);
-      g.add(mp.h_k, w_b, mp.s_store[b ^ 1], dz_next);
+    if (has_next) dz_next = dz_params(s + 1);
+    if (backward_grouping()) {
+      if (has_next) g.add(mp.h_k, w_b, mp.s_store[b ^ 1], dz_next);
+      if (!launch_group(FLCE_KERNEL_GEMM_BWD, g, sms, st)) return FLCE_ERR_CUDA;
+    } else {
+      Group gw(gm), gh(gm), gz(gm);
+      gw.add(mp.s_mn[b], mp.h_mn, mp.dw, dw);
+      gh.add(mp.s_k[b], mp.w_mn, mp.dh, dh);
+      if (!launch_group(FLCE_KERNEL_GEMM_DW, gw, sms, st)) return FLCE_ERR_CUDA;
+      if (!launch_group(FLCE_KERNEL_GEMM_DH, gh, sms, st)) return FLCE_ERR_CUDA;
+      if (has_next) {
+        gz.add(mp.h_k, w_b, mp.s_store[b ^ 1], dz_next);
+        if (!launch_group(FLCE_KERNEL_GEMM_DZ, gz, sms, st)) return FLCE_ERR_CUDA;
+      }
     }
-    if (!launch_group(FLCE_KERNEL_GEMM_BWD, g, sms, st)) return FLCE_ERR_CUDA;
     if (has_next && !count_skipped(dz_next)) return FLCE_ERR_CUDA;
     if (has_next && !dbias_item(s + 1)) return FLCE_ERR_CUDA;
   }

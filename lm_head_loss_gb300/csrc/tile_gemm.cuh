@@ -157,6 +157,13 @@ __device__ __forceinline__ bool kblock_skipped_group(const GemmParams& p, int mt
   return all;
 }
 
+// Runtime form of kblock_skipped_group for the epilogue.
+__device__ __forceinline__ bool kblock_skipped_n(const GemmParams& p, int mt_first, int group, int kb) {
+  for (int r = 0; r < group; ++r)
+    if (!kblock_skipped(p, mt_first + r, kb)) return false;
+  return true;
+}
+
 __device__ __forceinline__ void record_timeout(uint32_t* status, volatile uint32_t* abort_flag) {
   *abort_flag = 1u;
   atomicOr(status, kDevTimeout);
@@ -178,9 +185,11 @@ struct AccRelease {
   }
 };
 
+// `group` CTAs compute each tile group together (1, or 2 for the pair
+// kernel); a k-block left out of the MMAs is one every CTA of the group skips.
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtensorMap* tmOut, int mt, int nt,
                                               uint32_t taddr, int q, int lane, uint8_t* my_boxes, uint32_t& ebuf,
-                                              const AccRelease& rel) {
+                                              const AccRelease& rel, int group = 1) {
   const int r_local = q * 32 + lane;
   const int lrow = mt * kBM + r_local;         // local row of this launch
   if (mt >= p.m_tiles) {
@@ -333,7 +342,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
     // EPI_STORE / EPI_REDUCE
     bool all_skipped = p.skip_by_flags != 0;
     if (p.skip_by_flags) {
-      for (int kb = 0; kb < p.k_blocks && all_skipped; ++kb) all_skipped = kblock_skipped(p, mt, kb);
+      const int mt_first = mt - mt % group;
+      for (int kb = 0; kb < p.k_blocks && all_skipped; ++kb) all_skipped = kblock_skipped_n(p, mt_first, group, kb);
     }
     const float sc = __ldg(p.scale);
     if (!(all_skipped && p.mode == EPI_REDUCE)) {
@@ -451,8 +461,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
         const CUtensorMap* tmB = &L.tm_b[pi];
         tile_coords(p, tl, kCluster, rank, mt, nt);
         const int mt_first = mt - rank;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (kblock_skipped_group<kCluster>(p, mt_first, kb)) continue;
+        const bool may_skip = p.skip_by_flags != 0;
+        const int k_blocks = p.k_blocks;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (may_skip && kblock_skipped_group<kCluster>(p, mt_first, kb)) continue;
           if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
@@ -525,8 +537,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * kBN;
         uint32_t accumulate = 0;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (kblock_skipped_group<kCluster>(p, mt_first, kb)) continue;
+        const bool may_skip = p.skip_by_flags != 0;
+        const int k_blocks = p.k_blocks;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (may_skip && kblock_skipped_group<kCluster>(p, mt_first, kb)) continue;
           if (!ptx::mbar_wait_bounded(&full_bar[stage], phase, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
@@ -536,7 +550,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
           // In a cluster, a stage the group loads for the peer may still be
           // one this CTA's own tile skips: it then issues no MMA but still
           // releases the stage.
-          if (kCluster == 1 || !kblock_skipped(p, mt, kb)) {
+          if (kCluster == 1 || !may_skip || !kblock_skipped(p, mt, kb)) {
             const uint32_t a_addr = smem_base + stage * kStageBytes;
             const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll

@@ -11,8 +11,10 @@
 // multicast commits. Each CTA's epilogue warps read their own 128 TMEM lanes
 // and report to the even CTA that the accumulator buffer may be reused.
 //
-// Used for launches without gradient filtering (the pair computes both
-// halves of a group, so it cannot leave out one half's k-blocks).
+// With gradient filtering the pair leaves out a k-block only when both CTAs'
+// tiles skip it: the dW mask stays 128 rows x 256 vocabulary ids (both
+// halves of a dW group read the same dZ tile), the dH mask becomes 256 rows
+// x 256 ids (the two halves are two row tiles).
 #pragma once
 
 #include "tile_gemm.cuh"
@@ -25,6 +27,10 @@ constexpr uint32_t kPairStageBytes = kABytes + kPairBBytes;      // 32 KiB
 constexpr uint32_t kPairSmemBytes = 1024 + kPairStages * kPairStageBytes + kEpiBytes + kBarrierBytes;
 static_assert(kPairSmemBytes <= 232448, "shared memory of the pair kernel");
 
+// kSkip: some problem of the launch leaves out filtered k-blocks. Launches
+// without filtering use the kSkip = false instance, whose k-loops carry no
+// skip test at all.
+template <bool kSkip>
 __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const __grid_constant__ GemmLaunch L) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -93,7 +99,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
         const CUtensorMap* tmA = &L.tm_a[pi];
         const CUtensorMap* tmB = &L.tm_b[pi];
         tile_coords(p, tl, 2, rank, mt, nt);
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const bool may_skip = kSkip && p.skip_by_flags != 0;
+        const int k_blocks = p.k_blocks;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (kSkip && may_skip && kblock_skipped_group<2>(p, mt - rank, kb)) continue;
           if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
@@ -155,7 +164,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * kBN;
         uint32_t accumulate = 0;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        const bool a_mn = p.a_mn != 0, b_mn = p.b_mn != 0;
+        const bool may_skip = kSkip && p.skip_by_flags != 0;
+        const int k_blocks = p.k_blocks;
+        for (int kb = 0; kb < k_blocks; ++kb) {
+          if (kSkip && may_skip && kblock_skipped_group<2>(p, mt, kb)) continue;   // mt: the even CTA's m-tile
           if (!ptx::mbar_wait_bounded(&full_bar[stage], phase, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
@@ -166,10 +179,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
           const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
-            const uint64_t adesc = p.a_mn ? ptx::smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
-                                          : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
-            const uint64_t bdesc = p.b_mn ? ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
-                                          : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
+            const uint64_t adesc = a_mn ? ptx::smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                        : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
+            const uint64_t bdesc = b_mn ? ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                        : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
             ptx::mma_bf16_ss_pair(d_tmem, adesc, bdesc, idesc, accumulate);
             accumulate = 1;
           }
@@ -208,7 +221,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + buf * kBN + ((uint32_t)(q * 32) << 16);
       const AccRelease rel{&acc_empty[buf], ptx::map_to_rank(&acc_empty[buf], 0), !leader};
-      epilogue_tile(p, tmOut, mt, nt, taddr, q, lane, my_boxes, ebuf, rel);
+      epilogue_tile(p, tmOut, mt, nt, taddr, q, lane, my_boxes, ebuf, rel, 2);
     }
     if (lane == 0) ptx::bulk_wait_group<0>();
     __syncwarp();

@@ -181,15 +181,18 @@ def dW_rows(H, W, y, lse, vocab_ids, grad_loss: float = 1.0, ignore_index: int =
 
 def forward_backward_filtered(H, W, y, eps: float, tile_rows: int, tile_cols: int,
                               grad_loss: float = 1.0, ignore_index: int = IGNORE_INDEX,
-                              filter_dH: bool = True, filter_dW: bool = True):
+                              filter_dH: bool = True, filter_dW: bool = True, dH_tile_rows: int | None = None):
     """Gradient filtering of Cut Cross-Entropy Alg. 4, emulated in fp64.
 
     The dZ matrix is cut into tile_rows x tile_cols tiles aligned at 0; a tile
     whose unscaled gradient G = softmax - onehot has every |G| < eps (ignored
     rows count as G = 0) contributes nothing to dH or dW. filter_dH /
     filter_dW = False computes that gradient from the full G (the paper's
-    CCE-FullE / CCE-FullC variants). Returns the same tuple as
-    forward_backward plus the fraction of tiles skipped.
+    CCE-FullE / CCE-FullC variants). dH_tile_rows (a multiple of tile_rows,
+    default tile_rows) gives dH its own, taller mask: a tile_rows-high tile
+    then drops out of dH only when its whole dH_tile_rows-high block does.
+    Returns the same tuple as forward_backward plus the fraction of
+    tile_rows x tile_cols tiles skipped.
     """
     n, vocab = H.shape[0], W.shape[0]
     y = _check_targets(y, vocab, ignore_index)
@@ -199,19 +202,30 @@ def forward_backward_filtered(H, W, y, eps: float, tile_rows: int, tile_cols: in
     dH = np.zeros(H.shape, dtype=np.float64)
     dW = np.zeros(W.shape, dtype=np.float64)
     tiles = skipped = 0
-    for r0 in range(0, n, tile_rows):
-        r1 = min(n, r0 + tile_rows)
-        z = logits(H[r0:r1], W)
-        g = _dlogits_block(z, lse[r0:r1], y[r0:r1], 1.0, ignore_index)
-        g_full = g.copy()
+    hr = tile_rows if dH_tile_rows is None else dH_tile_rows
+    if hr % tile_rows != 0:
+        raise ValueError("dH_tile_rows must be a multiple of tile_rows")
+    for b0 in range(0, n, hr):
+        b1 = min(n, b0 + hr)
+        z = logits(H[b0:b1], W)
+        g_full = _dlogits_block(z, lse[b0:b1], y[b0:b1], 1.0, ignore_index)
+        g_w = g_full.copy()                      # dW mask: tile_rows x tile_cols
+        g_h = g_full.copy()                      # dH mask: hr x tile_cols
         for c0 in range(0, vocab, tile_cols):
             c1 = min(vocab, c0 + tile_cols)
-            tiles += 1
-            if np.all(np.abs(g[:, c0:c1]) < eps):
-                skipped += 1
-                g[:, c0:c1] = 0.0
-        dH[r0:r1] = ((g if filter_dH else g_full) * scale) @ W
-        dW += ((g if filter_dW else g_full) * scale).T @ H[r0:r1]
+            small = []
+            for r0 in range(0, b1 - b0, tile_rows):
+                r1 = min(b1 - b0, r0 + tile_rows)
+                tiles += 1
+                s_ = bool(np.all(np.abs(g_full[r0:r1, c0:c1]) < eps))
+                small.append(s_)
+                if s_:
+                    skipped += 1
+                    g_w[r0:r1, c0:c1] = 0.0
+            if all(small):
+                g_h[:, c0:c1] = 0.0
+        dH[b0:b1] = ((g_h if filter_dH else g_full) * scale) @ W
+        dW += ((g_w if filter_dW else g_full) * scale).T @ H[b0:b1]
     return lse, loss, dH, dW, count, skipped / max(tiles, 1)
 
 

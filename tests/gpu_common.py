@@ -5,6 +5,8 @@ Tolerances (filter off): mean-loss relative error <= 1e-3, per-row LSE
 absolute error <= 2e-3, dH and dW max absolute error <= 1e-2 * max|ref|.
 """
 
+import os
+
 import numpy as np
 import torch
 
@@ -83,3 +85,10 @@ def assert_parity(got, ref, loss_rel=LOSS_REL, lse_abs=LSE_ABS, grad_rel=GRAD_RE
     assert e.get("dH_rel", 0.0) <= grad_rel, e
     assert e.get("dW_rel", 0.0) <= grad_rel, e
     return e
+
+
+def dh_filter_rows() -> int:
+    """Height of the dH tile mask of the GEMM variant in use: the default pair
+    kernel leaves a dH k-block out only when both of its 128-row halves are
+    filtered; the 1-CTA and multicast variants filter 128-row tiles."""
+    return 128 if os.environ.get("FLCE_GEMM_MODE") in ("cta1", "multicast") else 256

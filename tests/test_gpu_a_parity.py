@@ -11,7 +11,8 @@ import torch
 import lm_head_loss_gb300 as flce
 import oracle
 import synth
-from gpu_common import (assert_parity, errors, gpu_fwd, gpu_fwd_bwd, oracle_full, small_inputs, to_device)
+from gpu_common import (assert_parity, dh_filter_rows, errors, gpu_fwd, gpu_fwd_bwd, oracle_full, small_inputs,
+                        to_device)
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
@@ -170,7 +171,8 @@ def test_filtered_gradient_matches_tile_mask_oracle():
     got = gpu_fwd_bwd(inp, filter_eps=eps)
     assert got["status"] == flce.Status.OK
     H64, W64 = oracle.inputs_f64(inp["H"], inp["W"])
-    lse, loss, dH, dW, _, frac = oracle.forward_backward_filtered(H64, W64, inp["y"], eps, 128, 256)
+    lse, loss, dH, dW, _, frac = oracle.forward_backward_filtered(H64, W64, inp["y"], eps, 128, 256,
+                                                                  dH_tile_rows=dh_filter_rows())
     full = oracle_full(inp)
     e_filt = errors(got, {"loss": loss, "lse": lse, "dH": dH, "dW": dW})
     e_full = errors(got, full)

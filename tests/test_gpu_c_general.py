@@ -8,7 +8,7 @@ import torch
 
 import lm_head_loss_gb300 as flce
 import oracle
-from gpu_common import GRAD_REL, LOSS_REL, LSE_ABS, small_inputs, to_device
+from gpu_common import GRAD_REL, LOSS_REL, LSE_ABS, dh_filter_rows, small_inputs, to_device
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
@@ -133,7 +133,7 @@ def test_filter_full_variants(flag, filter_dH, filter_dW):
     loss, lse, dH, dW = flce.forward_backward(H, W, y, filter_eps=eps, flags=flag)
     H64, W64 = oracle.inputs_f64(inp["H"], inp["W"])
     r = oracle.forward_backward_filtered(H64, W64, inp["y"], eps, 128, 256, filter_dH=filter_dH,
-                                         filter_dW=filter_dW)
+                                         filter_dW=filter_dW, dH_tile_rows=dh_filter_rows())
     assert r[5] > 0.5
     assert _rel(dH.cpu().numpy(), r[2]) <= GRAD_REL
     assert _rel(dW.cpu().numpy(), r[3]) <= GRAD_REL

@@ -289,3 +289,20 @@ def test_filter_full_variants():
     fe = oracle.forward_backward_filtered(H, W, y, 1e-3, 8, 16, filter_dH=False)
     assert np.array_equal(fc[2], f[2]) and np.max(np.abs(fc[3] - full[3])) < 1e-15
     assert np.array_equal(fe[3], f[3]) and np.max(np.abs(fe[2] - full[2])) < 1e-15
+
+
+def test_filter_taller_dH_mask():
+    H, W, y = _rand(35, 32, 6, 64, w_scale=2.0, ignore=(3,))
+    a = oracle.forward_backward_filtered(H, W, y, 1e-3, 8, 16)
+    b = oracle.forward_backward_filtered(H, W, y, 1e-3, 8, 16, dH_tile_rows=16)
+    full = oracle.forward_backward(H, W, y)
+    # dW and the skip statistic do not depend on the dH mask (dW up to the
+    # fp64 summation order of the row blocks).
+    assert np.max(np.abs(a[3] - b[3])) < 1e-15 and a[5] == b[5]
+    # A taller dH mask drops a subset of what the 8-row mask drops, so its dH
+    # is at least as close to the unfiltered one.
+    assert np.max(np.abs(b[2] - full[2])) <= np.max(np.abs(a[2] - full[2])) + 1e-15
+    c = oracle.forward_backward_filtered(H, W, y, 1e-3, 8, 16, dH_tile_rows=8)
+    assert np.array_equal(a[2], c[2])
+    with pytest.raises(ValueError):
+        oracle.forward_backward_filtered(H, W, y, 1e-3, 8, 16, dH_tile_rows=12)
