@@ -263,17 +263,21 @@ def run_ours(args, rank, world, local):
     cap = launches_per_step * args.steps
     prof = flce.LaunchProfiler(capacity=cap)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     with ClockSampler(local) as clocks:
         barrier()
         torch.cuda.synchronize()
         with prof:
             start.record(stream)
-            for _ in range(args.steps):
+            marks[0].record(stream)
+            for i in range(args.steps):
                 step()
+                marks[i + 1].record(stream)
             end.record(stream)
         torch.cuda.synchronize()
         barrier()
     total_ms = start.elapsed_time(end)
+    step_ms = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps))
     per_kind = prof.summary()
     clk = clocks.summary()
 
@@ -290,6 +294,7 @@ def run_ours(args, rank, world, local):
     peak = float(peaks["bf16_tflops_sustained"])
     step_tflops = flops_step / (ms_per_step / 1e3) / 1e12
 
+    fwd = run_forward_only(args, flce, torch, H, W, y, lse, loss, ws, prob, stream, N, D, V)
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -300,6 +305,9 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"dp{world} (independent batches, no collective)",
                    "l2": "no flush: W (592 MiB bf16) alone exceeds the 129 MB L2 every step"},
         "tflops": step_tflops,
+        "step_ms_median": statistics.median(step_ms),
+        "step_ms_p95": step_ms[min(len(step_ms) - 1, int(round(0.95 * (len(step_ms) - 1))))],
+        "forward_only": fwd,
         "pct_bf16_peak": 100.0 * step_tflops / peak,
         "pct_bf16_peak_burst": 100.0 * step_tflops / float(peaks["bf16_tflops"]),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -326,6 +334,22 @@ def run_ours(args, rank, world, local):
                                   "sample": f"first {rows} rows of the batch, full V and D, fp64 forward+backward, "
                                             f"{dt:.1f} s"}
     return result
+
+
+def run_forward_only(args, flce, torch, H, W, y, lse, loss, ws, prob, stream, N, D, V):
+    """flce_forward alone (per-row LSE and the loss; 2*N*V*D FLOPs), timed the same way."""
+    for _ in range(args.warmup):
+        if flce.flce_forward(prob, H, W, y, lse, loss, ws, stream=stream) != flce.Status.OK:
+            raise RuntimeError("flce_forward failed")
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        flce.flce_forward(prob, H, W, y, lse, loss, ws, stream=stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / args.steps
+    return {"ms_per_step": ms, "tokens_per_s": N / (ms / 1e3), "tflops": 2.0 * N * V * D / (ms / 1e3) / 1e12}
 
 
 def run_e2e(args, flce, torch, inp, prob, ws, outs, dev, stream, world, dist):
