@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     flce_forward_backward,
     flce_forward_ex,
     flce_forward_static_scratch,
+    flce_forward_workspace_bytes,
     flce_get_device_status,
     flce_get_filter_stats,
     flce_status_string,

@@ -66,6 +66,8 @@ def _load() -> ctypes.CDLL:
     prob = ctypes.POINTER(FlceProblem)
     lib.flce_workspace_bytes.argtypes = [prob]
     lib.flce_workspace_bytes.restype = sz
+    lib.flce_forward_workspace_bytes.argtypes = [prob]
+    lib.flce_forward_workspace_bytes.restype = sz
     lib.flce_forward.argtypes = [prob, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.flce_forward.restype = ctypes.c_int
     lib.flce_forward_backward.argtypes = [prob, vp, vp, vp, f32, vp, vp, vp, vp, vp, sz, vp]
@@ -122,6 +124,10 @@ def _nbytes(ws) -> int:
 
 def flce_workspace_bytes(problem: FlceProblem | None) -> int:
     return int(lib.flce_workspace_bytes(ctypes.byref(problem) if problem is not None else None))
+
+
+def flce_forward_workspace_bytes(problem: FlceProblem | None) -> int:
+    return int(lib.flce_forward_workspace_bytes(ctypes.byref(problem) if problem is not None else None))
 
 
 def flce_forward(problem, H, W, y, lse, loss, ws, ws_bytes: int | None = None, stream=None) -> Status:

@@ -34,8 +34,8 @@ class Workspace:
         self.device = torch.device(device if device is not None else "cuda")
         self.buf: torch.Tensor | None = None
 
-    def get(self, problem: B.FlceProblem) -> torch.Tensor:
-        need = B.flce_workspace_bytes(problem)
+    def get(self, problem: B.FlceProblem, forward_only: bool = False) -> torch.Tensor:
+        need = B.flce_forward_workspace_bytes(problem) if forward_only else B.flce_workspace_bytes(problem)
         if need == 0:
             raise B.FlceError(B.Status.ERR_INVALID_ARGUMENT, "flce_workspace_bytes")
         if self.buf is None or self.buf.numel() < need:
@@ -51,7 +51,7 @@ def forward(H, W, y, ignore_index: int = -100, workspace: Workspace | None = Non
     """Mean loss (fp32 scalar tensor) and per-row LSE [N] (fp32)."""
     _check_inputs(H, W, y)
     prob = _problem(H, W, ignore_index, 0.0, 0)
-    ws = (workspace or Workspace(H.device)).get(prob)
+    ws = (workspace or Workspace(H.device)).get(prob, forward_only=True)
     lse = torch.empty(H.shape[0], dtype=torch.float32, device=H.device)
     loss = torch.empty((), dtype=torch.float32, device=H.device)
     st = B.flce_forward(prob, H, W, y, lse, loss, ws, stream=stream)

@@ -898,8 +898,10 @@ static flce_status run_backward_any(const flce_problem& p, const Plan& pl, const
   return cudaGetLastError() == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
 }
 
+// forward_only: the call needs only the buffers in front of the backward's
+// flags and staging chunks (flce_forward_workspace_bytes).
 static flce_status check_common(const flce_problem* p, const void* H, const void* W, const int64_t* y,
-                                const float* loss, const void* ws, size_t ws_bytes) {
+                                const float* loss, const void* ws, size_t ws_bytes, bool forward_only = false) {
   if (!problem_ok(p)) return FLCE_ERR_INVALID_ARGUMENT;
   if (!loss || !ws) return FLCE_ERR_INVALID_ARGUMENT;
   if (p->n_rows > 0 && (!H || !y)) return FLCE_ERR_INVALID_ARGUMENT;
@@ -908,7 +910,8 @@ static flce_status check_common(const flce_problem* p, const void* H, const void
   if (!aligned(y, 8)) return FLCE_ERR_INVALID_ARGUMENT;
   if (p->hidden % 8 != 0) return FLCE_ERR_UNSUPPORTED;
   if (!aligned(H, 16) || !aligned(W, 16)) return FLCE_ERR_UNSUPPORTED;
-  if (ws_bytes < make_plan(*p).total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  const Plan pl = make_plan(*p);
+  if (ws_bytes < (forward_only ? pl.off_flags[0] : pl.total)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   return FLCE_OK;
 }
 
@@ -956,6 +959,11 @@ size_t flce_workspace_bytes(const flce_problem* p) {
   return make_plan(*p).total;
 }
 
+size_t flce_forward_workspace_bytes(const flce_problem* p) {
+  if (!problem_ok(p)) return 0;
+  return make_plan(*p).off_flags[0];
+}
+
 const char* flce_status_string(flce_status s) {
   switch (s) {
     case FLCE_OK: return "FLCE_OK";
@@ -971,7 +979,7 @@ const char* flce_status_string(flce_status s) {
 
 flce_status flce_forward(const flce_problem* p, const void* H, const void* W, const int64_t* y, float* lse,
                          float* loss, void* ws, size_t ws_bytes, void* stream) {
-  flce_status s = check_common(p, H, W, y, loss, ws, ws_bytes);
+  flce_status s = check_common(p, H, W, y, loss, ws, ws_bytes, true);
   if (s != FLCE_OK) return s;
   if (p->n_rows > 0 && !lse) return FLCE_ERR_INVALID_ARGUMENT;
   int sms = 0;
@@ -1016,7 +1024,7 @@ flce_status flce_forward_backward(const flce_problem* p, const void* H, const vo
 
 flce_status flce_forward_ex(const flce_problem* p, int32_t reduction, const void* H, const void* W, const float* bias,
                             const int64_t* y, float* lse, float* loss, void* ws, size_t ws_bytes, void* stream) {
-  flce_status s = check_common(p, H, W, y, loss, ws, ws_bytes);
+  flce_status s = check_common(p, H, W, y, loss, ws, ws_bytes, true);
   if (s != FLCE_OK) return s;
   if (reduction < FLCE_REDUCTION_MEAN || reduction > FLCE_REDUCTION_NONE) return FLCE_ERR_INVALID_ARGUMENT;
   if (p->n_rows > 0 && !lse) return FLCE_ERR_INVALID_ARGUMENT;

@@ -20,7 +20,7 @@ def test_library_exports_every_declared_symbol():
     assert set(declared) == {"flce_workspace_bytes", "flce_forward", "flce_forward_backward",
                              "flce_get_device_status", "flce_status_string", "flce_get_filter_stats",
                              "flce_profile_set", "flce_profile_count", "flce_forward_static_scratch",
-                             "flce_forward_ex", "flce_backward_ex"}
+                             "flce_forward_ex", "flce_backward_ex", "flce_forward_workspace_bytes"}
     out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
     for name in declared:
@@ -52,6 +52,19 @@ def test_compaction_workspace_is_linear_in_rows():
     base = flce.flce_workspace_bytes(flce.make_problem(8192, 2048, 151552))
     comp = flce.flce_workspace_bytes(flce.make_problem(8192, 2048, 151552, flags=flce.FLAG_COMPACT_IGNORED))
     assert 0 < comp - base <= 8192 * 2048 * 6 + 8192 * 28 + 8 * 1024
+
+
+def test_forward_workspace_is_the_front_of_the_full_one():
+    p = flce.make_problem(8192, 2048, 151552)
+    fwd, full = flce.flce_forward_workspace_bytes(p), flce.flce_workspace_bytes(p)
+    assert 0 < fwd < full / 4
+    assert fwd < 8192 * 151552 * 2 / 50
+    nb = fwd
+    assert flce.flce_forward(p, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws_bytes=nb - 1, stream=0) == \
+        Status.ERR_WORKSPACE_TOO_SMALL
+    assert flce.flce_forward_backward(p, FAKE, FAKE, FAKE, 1.0, None, FAKE, FAKE, FAKE, FAKE, ws_bytes=nb,
+                                      stream=0) == Status.ERR_WORKSPACE_TOO_SMALL
+    assert flce.flce_forward_workspace_bytes(None) == 0
 
 
 def test_workspace_bytes_rejects_bad_problems():
@@ -86,7 +99,7 @@ def test_host_argument_checks_return_before_any_launch():
     assert _fwd(good, ws=FAKE + 16) == Status.ERR_INVALID_ARGUMENT          # ws not 256-byte aligned
     assert _fwd(good, y=FAKE + 4) == Status.ERR_INVALID_ARGUMENT            # int64 targets misaligned
     assert _fwd(good, H=FAKE + 8) == Status.ERR_UNSUPPORTED                 # TMA needs 16-byte alignment
-    assert _fwd(good, nb=flce.flce_workspace_bytes(good) - 1) == Status.ERR_WORKSPACE_TOO_SMALL
+    assert _fwd(good, nb=flce.flce_forward_workspace_bytes(good) - 1) == Status.ERR_WORKSPACE_TOO_SMALL
     assert _fwd(flce.make_problem(16, 60, 100)) == Status.ERR_UNSUPPORTED   # D % 8 != 0
     assert _fwd(flce.make_problem(16, 64, 100, flags=0x10)) == Status.ERR_INVALID_ARGUMENT
     assert _fwd(flce.make_problem(16, 64, 100, filter_eps=float("nan"))) == Status.ERR_INVALID_ARGUMENT

@@ -212,3 +212,32 @@ def test_cuda_graph_capture_and_replay():
         torch.cuda.synchronize()
         for a, b in zip(outs, eager):
             assert torch.equal(a, b)
+
+
+def test_calls_allocate_no_device_memory():
+    # After a first call has set the device up, further calls of every entry
+    # point leave the device's free memory exactly where it was: the caller's
+    # workspace is the only scratch the library uses.
+    n, d, v = 3000, 256, 20000
+    inp = small_inputs(n, d, v, seed=91, targets="zipf")
+    H, W, y = to_device(inp)
+    prob = flce.make_problem(n, d, v)
+    ws = torch.empty(flce.flce_workspace_bytes(prob), dtype=torch.uint8, device="cuda")
+    fws = torch.empty(flce.flce_forward_workspace_bytes(prob), dtype=torch.uint8, device="cuda")
+    loss, lse = torch.empty((), device="cuda"), torch.empty(n, device="cuda")
+    dH, dW = torch.empty(n, d, device="cuda"), torch.empty(v, d, device="cuda")
+
+    def calls():
+        assert flce.flce_forward_backward(prob, H, W, y, 1.0, lse, loss, dH, dW, ws) == flce.Status.OK
+        assert flce.flce_forward(prob, H, W, y, lse, loss, fws) == flce.Status.OK
+
+    calls()
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        calls()
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert flce.flce_get_device_status(fws) == flce.Status.OK
+    ref = oracle_full(inp)
+    assert abs(loss.item() - ref["loss"]) <= 1e-3 * abs(ref["loss"])
