@@ -7,6 +7,7 @@ arm use it. It shares no code with the CUDA path.
 
 from .flce_oracle import (  # noqa: F401
     IGNORE_INDEX,
+    average_logits,
     dlogits,
     dH_rows,
     dW_rows,
@@ -20,4 +21,5 @@ from .flce_oracle import (  # noqa: F401
     loss_value,
     lse_rows,
     valid_count,
+    vocabulary_order,
 )

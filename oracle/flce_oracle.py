@@ -179,9 +179,43 @@ def dW_rows(H, W, y, lse, vocab_ids, grad_loss: float = 1.0, ignore_index: int =
     return scale * (p.T @ H)
 
 
+def average_logits(H, W, y, bias=None, ignore_index: int = IGNORE_INDEX) -> np.ndarray:
+    """Average logit of every vocabulary entry over the valid rows.
+
+    Cut Cross-Entropy, Sec. 4.3 "Vocabulary sorting": the forward pass
+    accumulates, per token, its logit averaged over the batch, and the
+    backward groups the vocabulary by that average. Read here as
+    a_v = sum_{valid n} z_nv / count, with z_nv = H_n W_v^T (+ b_v); ignored
+    rows carry no gradient, so they take no part; all zero when count = 0.
+    Computed from the logits themselves, a row block at a time.
+    """
+    n, vocab = H.shape[0], W.shape[0]
+    y = _check_targets(y, vocab, ignore_index)
+    valid = y != ignore_index
+    count = int(valid.sum())
+    total = np.zeros(vocab, dtype=np.float64)
+    for r0, r1 in _row_blocks(n, vocab):
+        z = logits(H[r0:r1], W)
+        if bias is not None:
+            z = z + np.asarray(bias, dtype=np.float64)[None, :]
+        total += z[valid[r0:r1]].sum(axis=0)
+    return total / count if count > 0 else total
+
+
+def vocabulary_order(avg: np.ndarray) -> np.ndarray:
+    """Vocabulary ids by decreasing average logit, equal averages in id order.
+
+    order[i] is the id placed at sorted position i; the backward then cuts
+    the sorted vocabulary into blocks, so ids of similar average logit share
+    a block (Cut Cross-Entropy, Sec. 4.3 "Vocabulary sorting").
+    """
+    return np.argsort(-np.asarray(avg, dtype=np.float64), kind="stable")
+
+
 def forward_backward_filtered(H, W, y, eps: float, tile_rows: int, tile_cols: int,
                               grad_loss: float = 1.0, ignore_index: int = IGNORE_INDEX,
-                              filter_dH: bool = True, filter_dW: bool = True, dH_tile_rows: int | None = None):
+                              filter_dH: bool = True, filter_dW: bool = True, dH_tile_rows: int | None = None,
+                              vocab_order=None):
     """Gradient filtering of Cut Cross-Entropy Alg. 4, emulated in fp64.
 
     The dZ matrix is cut into tile_rows x tile_cols tiles aligned at 0; a tile
@@ -191,11 +225,34 @@ def forward_backward_filtered(H, W, y, eps: float, tile_rows: int, tile_cols: in
     CCE-FullE / CCE-FullC variants). dH_tile_rows (a multiple of tile_rows,
     default tile_rows) gives dH its own, taller mask: a tile_rows-high tile
     then drops out of dH only when its whole dH_tile_rows-high block does.
+    vocab_order (a permutation of the ids, e.g. vocabulary_order's) lays the
+    columns out in that order before the tiles are cut, so column block j
+    holds ids vocab_order[j*tile_cols : (j+1)*tile_cols] (Sec. 4.3,
+    "Vocabulary sorting"); dW is returned in id order.
     Returns the same tuple as forward_backward plus the fraction of
     tile_rows x tile_cols tiles skipped.
     """
     n, vocab = H.shape[0], W.shape[0]
     y = _check_targets(y, vocab, ignore_index)
+    if vocab_order is not None:
+        order = np.asarray(vocab_order, dtype=np.int64)
+        if order.shape != (vocab,) or not np.array_equal(np.sort(order), np.arange(vocab)):
+            raise ValueError("vocab_order must be a permutation of the vocabulary ids")
+        position = np.empty(vocab, dtype=np.int64)
+        position[order] = np.arange(vocab)
+        y_sorted = np.where(y == ignore_index, y, position[np.where(y == ignore_index, 0, y)])
+        if ignore_index >= 0:
+            # keep ignored rows ignored even where a position equals ignore_index
+            y_sorted = np.where(y == ignore_index, -1, y_sorted)
+            ignore_sorted = -1
+        else:
+            ignore_sorted = ignore_index
+        lse, loss, dH, dW_sorted, count, frac = forward_backward_filtered(
+            H, W[order], y_sorted, eps, tile_rows, tile_cols, grad_loss, ignore_sorted, filter_dH, filter_dW,
+            dH_tile_rows)
+        dW = np.empty_like(dW_sorted)
+        dW[order] = dW_sorted
+        return lse, loss, dH, dW, count, frac
     count = valid_count(y, ignore_index)
     scale = grad_loss / max(count, 1)
     lse, loss, _ = forward(H, W, y, ignore_index)

@@ -306,3 +306,119 @@ def test_filter_taller_dH_mask():
     assert np.array_equal(a[2], c[2])
     with pytest.raises(ValueError):
         oracle.forward_backward_filtered(H, W, y, 1e-3, 8, 16, dH_tile_rows=12)
+
+
+# ---- vocabulary sorting (Cut Cross-Entropy, Sec. 4.3 "Vocabulary sorting")
+
+def test_average_logits_closed_forms():
+    n, d, v = 9, 6, 17
+    H, W, y = _rand(21, n, d, v, ignore=(0, 4, 7))
+    valid = y != IGN
+    # Linearity: the mean of z_nv over valid rows is W_v . mean(H_valid).
+    a = oracle.average_logits(H, W, y)
+    assert np.max(np.abs(a - W @ H[valid].mean(axis=0))) < 1e-13
+    # A bias adds b_v to every logit, hence to the average.
+    b = np.linspace(-2.0, 3.0, v)
+    assert np.max(np.abs(oracle.average_logits(H, W, y, bias=b) - (a + b))) < 1e-13
+    # W = 0: every logit is zero.
+    assert np.all(oracle.average_logits(H, np.zeros_like(W), y) == 0.0)
+    # No valid row: all zero.
+    assert np.all(oracle.average_logits(H, W, np.full(n, IGN)) == 0.0)
+
+
+def test_average_logits_ignore_ignored_rows():
+    n, d, v = 8, 5, 11
+    H, W, y = _rand(22, n, d, v, ignore=(1, 6))
+    a = oracle.average_logits(H, W, y)
+    H2 = H.copy()
+    H2[[1, 6]] = 1e3 * np.arange(1, d + 1)
+    assert np.array_equal(oracle.average_logits(H2, W, y), a)
+    # Changing a valid row does move the average of every non-zero W row.
+    H3 = H.copy()
+    H3[2] += 1.0
+    assert np.all(np.abs(oracle.average_logits(H3, W, y) - a) > 1e-6)
+
+
+def test_average_logits_permute_with_the_vocabulary():
+    n, d, v = 6, 4, 10
+    H, W, y = _rand(23, n, d, v, ignore=(3,))
+    perm = np.random.default_rng(5).permutation(v)
+    inv = np.argsort(perm)
+    y2 = np.where(y == IGN, IGN, inv[np.where(y == IGN, 0, y)])
+    assert np.max(np.abs(oracle.average_logits(H, W[perm], y2) - oracle.average_logits(H, W, y)[perm])) < 1e-13
+
+
+def test_vocabulary_order_is_descending_and_stable():
+    a = np.array([0.5, 2.0, -1.0, 2.0, 0.5, 7.0, -0.0, 0.0, -1.0])
+    order = oracle.vocabulary_order(a)
+    brute = sorted(range(len(a)), key=lambda i: (-a[i], i))
+    assert list(order) == brute
+    assert list(order) == [5, 1, 3, 0, 4, 6, 7, 2, 8]
+
+
+def _interleaved_case():
+    # Even ids get a logit far below the rest for every row, odd ids sit
+    # near zero: in id order every 2-wide column block mixes one of each.
+    n, d, v = 6, 3, 8
+    H = np.ones((n, d))
+    H[:, 1] = np.linspace(-0.2, 0.2, n)
+    W = np.zeros((v, d))
+    W[0::2, 0] = -15.0
+    W[1::2, 2] = np.linspace(0.1, 0.4, v // 2)
+    y = np.array([1, 3, 5, 7, 1, IGN], dtype=np.int64)
+    return H, W, y
+
+
+def test_sorting_groups_negligible_columns_into_skippable_tiles():
+    H, W, y = _interleaved_case()
+    eps = 2.0 ** -12
+    *_, frac_id = oracle.forward_backward_filtered(H, W, y, eps, 3, 2)
+    order = oracle.vocabulary_order(oracle.average_logits(H, W, y))
+    assert sorted(order[:4]) == [1, 3, 5, 7]
+    lse, loss, dH, dW, count, frac_sorted = oracle.forward_backward_filtered(H, W, y, eps, 3, 2, vocab_order=order)
+    assert frac_id == 0.0
+    assert frac_sorted == 0.5          # the two all-even column blocks, both row blocks
+    # The skipped G are all below eps, so the result stays within the filter's error bound.
+    ref = oracle.forward_backward(H, W, y)
+    assert abs(loss - ref[1]) < 1e-15 and np.max(np.abs(lse - ref[0])) < 1e-15
+    assert np.max(np.abs(dH - ref[2])) < 2 * eps * 15 and np.max(np.abs(dW - ref[3])) < 2 * eps
+    assert not np.array_equal(dW, ref[3])
+
+
+def test_vocab_order_equivariance_and_degenerate_cases():
+    n, d, v = 10, 4, 12
+    H, W, y = _rand(24, n, d, v, w_scale=2.0, ignore=(2, 9))
+    eps = 0.01
+    perm = np.random.default_rng(6).permutation(v)
+    # Identity order is the plain tile mask.
+    a = oracle.forward_backward_filtered(H, W, y, eps, 4, 3)
+    b = oracle.forward_backward_filtered(H, W, y, eps, 4, 3, vocab_order=np.arange(v))
+    for x, z in zip(a, b):
+        assert np.array_equal(np.asarray(x), np.asarray(z))
+    # Sorting by `perm` equals relabelling the vocabulary by hand.
+    inv = np.argsort(perm)
+    y2 = np.where(y == IGN, IGN, inv[np.where(y == IGN, 0, y)])
+    hand = oracle.forward_backward_filtered(H, W[perm], y2, eps, 4, 3)
+    got = oracle.forward_backward_filtered(H, W, y, eps, 4, 3, vocab_order=perm)
+    assert got[5] == hand[5]
+    assert np.max(np.abs(got[2] - hand[2])) < 1e-13
+    assert np.max(np.abs(got[3][perm] - hand[3])) < 1e-13
+    # eps = 0 filters nothing: any order gives the unfiltered result.
+    ref = oracle.forward_backward(H, W, y)
+    got0 = oracle.forward_backward_filtered(H, W, y, 0.0, 4, 3, vocab_order=perm)
+    assert got0[5] == 0.0
+    assert np.max(np.abs(got0[2] - ref[2])) < 1e-13 and np.max(np.abs(got0[3] - ref[3])) < 1e-13
+    with pytest.raises(ValueError):
+        oracle.forward_backward_filtered(H, W, y, eps, 4, 3, vocab_order=np.zeros(v, dtype=np.int64))
+
+
+def test_vocab_order_with_ignore_index_inside_the_vocabulary():
+    n, d, v = 8, 4, 9
+    H, W, _ = _rand(25, n, d, v)
+    y = np.array([0, 4, 4, 8, 2, 4, 1, 7], dtype=np.int64)      # 4 is the ignore index
+    perm = np.random.default_rng(7).permutation(v)
+    ref = oracle.forward_backward(H, W, y, ignore_index=4)
+    got = oracle.forward_backward_filtered(H, W, y, 0.0, 4, 3, ignore_index=4, vocab_order=perm)
+    assert got[4] == ref[4] == 5
+    assert abs(got[1] - ref[1]) < 1e-14
+    assert np.max(np.abs(got[2] - ref[2])) < 1e-13 and np.max(np.abs(got[3] - ref[3])) < 1e-13
