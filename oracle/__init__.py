@@ -7,12 +7,14 @@ arm use it. It shares no code with the CUDA path.
 
 from .flce_oracle import (  # noqa: F401
     IGNORE_INDEX,
+    adamw_step,
     average_logits,
     dlogits,
     dH_rows,
     dW_rows,
     forward,
     forward_backward,
+    forward_backward_adamw,
     forward_backward_ex,
     forward_backward_filtered,
     inputs_f64,

@@ -339,3 +339,46 @@ def forward_backward_ex(H, W, y, bias=None, reduction: str = "mean", grad=1.0,
     else:
         loss = float(rows_loss.sum()) / max(count, 1)
     return {"lse": lse, "loss": loss, "count": count, "dH": dH, "dW": dW, "db": db}
+
+
+def adamw_step(param, grad, m, v, step: int, lr: float, beta1: float, beta2: float, eps: float,
+               weight_decay: float):
+    """One AdamW step, elementwise in fp64; returns the new (param, m, v).
+
+    The optimizer the FORGE explainer fuses into the weight-gradient tiles
+    ("FORGE: Fused On-Register Gradient Elimination for Memory-Efficient LLM
+    Training", Sec. 2, core mechanism: AdamW named as the example). The page
+    prints no formula; this is AdamW with decoupled weight decay as
+    Loshchilov and Hutter define it and torch.optim.AdamW computes it:
+        param <- param * (1 - lr * weight_decay)
+        m <- beta1 m + (1 - beta1) g,   v <- beta2 v + (1 - beta2) g^2
+        param <- param - lr * (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps)
+    with t = step >= 1, the step being taken.
+    """
+    if step < 1:
+        raise ValueError("step counts from 1")
+    p = np.asarray(param, dtype=np.float64) * (1.0 - lr * weight_decay)
+    g = np.asarray(grad, dtype=np.float64)
+    m = beta1 * np.asarray(m, dtype=np.float64) + (1.0 - beta1) * g
+    v = beta2 * np.asarray(v, dtype=np.float64) + (1.0 - beta2) * g * g
+    m_hat = m / (1.0 - beta1 ** step)
+    v_hat = v / (1.0 - beta2 ** step)
+    p = p - lr * m_hat / (np.sqrt(v_hat) + eps)
+    return p, m, v
+
+
+def forward_backward_adamw(H, W, y, master, m, v, hparams: dict, grad_loss: float = 1.0,
+                           ignore_index: int = IGNORE_INDEX):
+    """The LM-head step with W's AdamW update fused into its gradient.
+
+    FORGE applies the optimizer to each weight-gradient tile as soon as the
+    tile is complete, so the gradient is never stored; for an elementwise
+    optimizer the page states the result equals the usual two-phase step
+    (Sec. 2, exactness). The oracle is therefore the two-phase step: dW of
+    forward_backward (on the bf16 W the forward used), then adamw_step on
+    the fp32 master weights. Returns a dict with lse, loss, count, dH and
+    the new master, m and v.
+    """
+    lse, loss, dH, dW, count = forward_backward(H, W, y, grad_loss=grad_loss, ignore_index=ignore_index)
+    p, m2, v2 = adamw_step(master, dW, m, v, **hparams)
+    return {"lse": lse, "loss": loss, "count": count, "dH": dH, "dW": dW, "master": p, "m": m2, "v": v2}

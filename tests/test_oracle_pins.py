@@ -422,3 +422,66 @@ def test_vocab_order_with_ignore_index_inside_the_vocabulary():
     assert got[4] == ref[4] == 5
     assert abs(got[1] - ref[1]) < 1e-14
     assert np.max(np.abs(got[2] - ref[2])) < 1e-13 and np.max(np.abs(got[3] - ref[3])) < 1e-13
+
+
+# ---- AdamW fused into the weight gradient (FORGE explainer, Sec. 2)
+
+_HP = {"lr": 1e-3, "beta1": 0.9, "beta2": 0.95, "eps": 1e-8, "weight_decay": 0.1}
+
+
+def test_adamw_matches_torch_optim_over_several_steps():
+    rng = np.random.default_rng(31)
+    p0 = rng.standard_normal((7, 5))
+    grads = [rng.standard_normal((7, 5)) for _ in range(4)]
+    tp = torch.tensor(p0, dtype=torch.float64, requires_grad=True)
+    opt = torch.optim.AdamW([tp], lr=_HP["lr"], betas=(_HP["beta1"], _HP["beta2"]), eps=_HP["eps"],
+                            weight_decay=_HP["weight_decay"])
+    p, m, v = p0, np.zeros_like(p0), np.zeros_like(p0)
+    for t, g in enumerate(grads, start=1):
+        tp.grad = torch.tensor(g, dtype=torch.float64)
+        opt.step()
+        p, m, v = oracle.adamw_step(p, g, m, v, t, **_HP)
+        assert np.max(np.abs(p - tp.detach().numpy())) < 1e-15
+    st = opt.state[tp]
+    assert np.max(np.abs(m - st["exp_avg"].numpy())) < 1e-15
+    assert np.max(np.abs(v - st["exp_avg_sq"].numpy())) < 1e-15
+
+
+def test_adamw_first_step_closed_form():
+    # From zero moments the bias-corrected ratio is g / (|g| + eps).
+    rng = np.random.default_rng(32)
+    p0, g = rng.standard_normal(20), rng.standard_normal(20)
+    p, m, v = oracle.adamw_step(p0, g, np.zeros(20), np.zeros(20), 1, **_HP)
+    lr, wd, eps = _HP["lr"], _HP["weight_decay"], _HP["eps"]
+    assert np.max(np.abs(p - (p0 * (1 - lr * wd) - lr * g / (np.abs(g) + eps)))) < 1e-15
+    assert np.max(np.abs(m - (1 - _HP["beta1"]) * g)) < 1e-15
+    assert np.max(np.abs(v - (1 - _HP["beta2"]) * g * g)) < 1e-15
+    # No learning rate: the parameters stay; the moments still move.
+    p2, m2, _ = oracle.adamw_step(p0, g, np.zeros(20), np.zeros(20), 1, **{**_HP, "lr": 0.0})
+    assert np.array_equal(p2, p0) and np.any(m2 != 0)
+    with pytest.raises(ValueError):
+        oracle.adamw_step(p0, g, m, v, 0, **_HP)
+
+
+def test_fused_step_equals_gradient_then_optimizer():
+    n, d, v = 9, 6, 13
+    H, W, y = _rand(33, n, d, v, ignore=(4,))
+    rng = np.random.default_rng(34)
+    master, m0, v0 = W + 1e-3 * rng.standard_normal(W.shape), rng.standard_normal(W.shape), rng.random(W.shape)
+    hp = {**_HP, "step": 3}
+    r = oracle.forward_backward_adamw(H, W, y, master, m0, v0, hp, grad_loss=0.5)
+    lse, loss, dH, dW, count = oracle.forward_backward(H, W, y, grad_loss=0.5)
+    # dW of a library autograd pass, then the library optimizer.
+    Wt = torch.tensor(W, requires_grad=True)
+    ce = torch.nn.functional.cross_entropy(torch.tensor(H) @ Wt.T, torch.tensor(y), ignore_index=IGN) * 0.5
+    ce.backward()
+    assert np.max(np.abs(Wt.grad.numpy() - dW)) < 1e-14
+    tp = torch.tensor(master, requires_grad=True)
+    opt = torch.optim.AdamW([tp], lr=hp["lr"], betas=(hp["beta1"], hp["beta2"]), eps=hp["eps"],
+                            weight_decay=hp["weight_decay"])
+    opt.state[tp] = {"step": torch.tensor(2.0, dtype=torch.float64), "exp_avg": torch.tensor(m0),
+                     "exp_avg_sq": torch.tensor(v0)}
+    tp.grad = Wt.grad
+    opt.step()
+    assert np.max(np.abs(r["master"] - tp.detach().numpy())) < 1e-14
+    assert r["count"] == count and abs(r["loss"] - loss) < 1e-15
