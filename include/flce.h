@@ -103,6 +103,22 @@ typedef struct {
  * grows by about 6*N*D + 28*N bytes. */
 #define FLCE_FLAG_COMPACT_IGNORED 0x8u
 
+/* Vocabulary sorting of Cut Cross-Entropy (Sec. 4.3, "Vocabulary sorting"):
+ * the backward visits the vocabulary in order of decreasing average logit,
+ * so that ids of similar average share a 256-id block and the gradient
+ * filter (filter_eps > 0) finds more blocks it can leave out.
+ *   The average logit of id v is the mean of z_nv (+ b_v) over the
+ *   non-ignored rows, 0 when no row is valid. It is formed as
+ *   W_v . mean(H over valid rows) (+ b_v), the same value by linearity,
+ *   in fp32; ids of equal average keep their id order.
+ *   The backward runs on a copy of W with its rows in that order (kept in
+ *   the workspace, which grows by V*D*2 + 28*V + 8*N + 1028*D bytes) and
+ *   writes dW and d(bias) back to the caller's buffers in id order. With
+ *   filtering off the results equal those of the unsorted backward up to
+ *   fp32 summation order. The forward ignores the flag.
+ *   flce_get_vocab_order reads back the order and the averages. */
+#define FLCE_FLAG_SORT_VOCAB 0x10u
+
 /* Bytes of device workspace every compute call below (flce_forward,
  * flce_forward_backward, flce_forward_ex, flce_backward_ex) needs for
  * problem *p (0 if p is NULL or invalid). Pure host arithmetic; needs no GPU. */
@@ -177,6 +193,16 @@ const char* flce_status_string(flce_status s);
  * filtering was off. */
 flce_status flce_get_filter_stats(void* ws, void* stream, double* skipped_fraction);
 
+/* The vocabulary order of the most recent backward that ran problem *p with
+ * FLCE_FLAG_SORT_VOCAB on workspace `ws`: order[i] (device int32 [V]) is
+ * the id visited at position i, and avg_logit (device float [V], may be
+ * NULL) the average logit of every id, in id order. Both are copied from
+ * the workspace on `stream` (asynchronous, no synchronisation).
+ * FLCE_ERR_INVALID_ARGUMENT if p is invalid, lacks the flag, or a pointer
+ * is NULL or order is not 4-byte aligned. */
+flce_status flce_get_vocab_order(const flce_problem* p, const void* ws, int32_t* order, float* avg_logit,
+                                 void* stream);
+
 /* flce_forward without a caller-provided workspace, for callers that cannot
  * allocate device memory at the point they need the loss: for example a
  * plugin of an inference or training engine whose execute step must not
@@ -221,6 +247,9 @@ flce_status flce_forward_static_scratch(const flce_problem* p, const void* H, co
 #define FLCE_KERNEL_GEMM_BWD 8 /* one launch: dW and dH of a chunk + dZ of the next chunk */
 #define FLCE_KERNEL_DBIAS 9
 #define FLCE_KERNEL_SET_SCALE 10
+#define FLCE_KERNEL_VOCAB_KEYS 11   /* average logits: column sums of H, their mean, W . mean */
+#define FLCE_KERNEL_VOCAB_SORT 12   /* stable radix sort of the averages, inverse order */
+#define FLCE_KERNEL_VOCAB_GATHER 13 /* W, bias and targets rearranged in the sorted order */
 flce_status flce_profile_set(void** events, int32_t* kinds, int32_t cap);
 int32_t flce_profile_count(void);
 

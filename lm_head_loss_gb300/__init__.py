@@ -9,6 +9,7 @@ from ._binding import (  # noqa: F401
     FLAG_COMPACT_IGNORED,
     FLAG_FILTER_FULL_DH,
     FLAG_FILTER_FULL_DW,
+    FLAG_SORT_VOCAB,
     FLAG_TEST_SHORT_WAITS,
     REDUCTIONS,
     FlceError,
@@ -24,6 +25,7 @@ from ._binding import (  # noqa: F401
     flce_forward_workspace_bytes,
     flce_get_device_status,
     flce_get_filter_stats,
+    flce_get_vocab_order,
     flce_status_string,
     flce_workspace_bytes,
     lib,

@@ -32,6 +32,7 @@ FLAG_TEST_SHORT_WAITS = 0x1
 FLAG_FILTER_FULL_DW = 0x2
 FLAG_FILTER_FULL_DH = 0x4
 FLAG_COMPACT_IGNORED = 0x8
+FLAG_SORT_VOCAB = 0x10
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 
@@ -78,6 +79,8 @@ def _load() -> ctypes.CDLL:
     lib.flce_status_string.restype = ctypes.c_char_p
     lib.flce_get_filter_stats.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_double)]
     lib.flce_get_filter_stats.restype = ctypes.c_int
+    lib.flce_get_vocab_order.argtypes = [prob, vp, vp, vp, vp]
+    lib.flce_get_vocab_order.restype = ctypes.c_int
     lib.flce_forward_ex.argtypes = [prob, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.flce_forward_ex.restype = ctypes.c_int
     lib.flce_backward_ex.argtypes = [prob, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -184,8 +187,16 @@ def flce_get_filter_stats(ws, stream=None) -> float:
     return out.value
 
 
+def flce_get_vocab_order(problem, ws, order, avg_logit=None, stream=None) -> Status:
+    """Copy the sorted vocabulary order (int32 [V]) and, if given, the average
+    logits (float [V]) of the last sorted backward out of the workspace."""
+    return Status(lib.flce_get_vocab_order(ctypes.byref(problem) if problem is not None else None, _addr(ws),
+                                           _addr(order), _addr(avg_logit), _stream(stream)))
+
+
 KERNEL_KINDS = {0: "gemm_lse", 1: "gemm_dz", 2: "gemm_dw", 3: "gemm_dh", 4: "prep", 5: "combine",
-                6: "finalize", 7: "filter_stats", 8: "gemm_bwd", 9: "dbias", 10: "set_scale"}
+                6: "finalize", 7: "filter_stats", 8: "gemm_bwd", 9: "dbias", 10: "set_scale",
+                11: "vocab_keys", 12: "vocab_sort", 13: "vocab_gather"}
 
 
 class LaunchProfiler:

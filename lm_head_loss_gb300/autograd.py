@@ -36,7 +36,7 @@ def _workspace(device: torch.device) -> Workspace:
 
 class _LinearCrossEntropy(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, hidden, weight, bias, target, ignore_index, reduction, filter_eps):
+    def forward(ctx, hidden, weight, bias, target, ignore_index, reduction, filter_eps, flags):
         _check_inputs(hidden, weight, target)
         if bias is not None:
             if bias.dtype != torch.float32 or not bias.is_cuda or bias.shape != (weight.shape[0],):
@@ -44,7 +44,7 @@ class _LinearCrossEntropy(torch.autograd.Function):
             bias = bias.contiguous()
         red = B.REDUCTIONS[reduction]
         n, d, v = hidden.shape[0], hidden.shape[1], weight.shape[0]
-        prob = B.make_problem(n, d, v, ignore_index, filter_eps, 0)
+        prob = B.make_problem(n, d, v, ignore_index, filter_eps, flags)
         ws = _workspace(hidden.device)
         buf = ws.get(prob)
         lse = torch.empty(n, dtype=torch.float32, device=hidden.device)
@@ -53,7 +53,7 @@ class _LinearCrossEntropy(torch.autograd.Function):
         if st != B.Status.OK:
             raise B.FlceError(st, "flce_forward_ex")
         ctx.save_for_backward(hidden, weight, bias, target, lse)
-        ctx.red, ctx.ignore_index, ctx.filter_eps = red, ignore_index, filter_eps
+        ctx.red, ctx.ignore_index, ctx.filter_eps, ctx.flags = red, ignore_index, filter_eps, flags
         ctx.mark_non_differentiable(lse)
         return loss, lse
 
@@ -61,7 +61,7 @@ class _LinearCrossEntropy(torch.autograd.Function):
     def backward(ctx, grad_loss, grad_lse):
         hidden, weight, bias, target, lse = ctx.saved_tensors
         n, d, v = hidden.shape[0], hidden.shape[1], weight.shape[0]
-        prob = B.make_problem(n, d, v, ctx.ignore_index, ctx.filter_eps, 0)
+        prob = B.make_problem(n, d, v, ctx.ignore_index, ctx.filter_eps, ctx.flags)
         buf = _workspace(hidden.device).get(prob)
         grad = grad_loss.to(torch.float32).contiguous().reshape(-1)
         dH = torch.empty(hidden.shape, dtype=torch.float32, device=hidden.device)
@@ -70,23 +70,27 @@ class _LinearCrossEntropy(torch.autograd.Function):
         st = B.flce_backward_ex(prob, ctx.red, hidden, weight, bias, target, lse, grad, dH, dW, db, buf)
         if st != B.Status.OK:
             raise B.FlceError(st, "flce_backward_ex")
-        return dH, dW, db, None, None, None, None
+        return dH, dW, db, None, None, None, None, None
 
 
 def linear_cross_entropy(hidden: torch.Tensor, weight: torch.Tensor, target: torch.Tensor,
                          bias: torch.Tensor | None = None, ignore_index: int = -100, reduction: str = "mean",
-                         filter_eps: float = 0.0, return_lse: bool = False):
+                         filter_eps: float = 0.0, return_lse: bool = False, sort_vocab: bool = False):
     """Cross-entropy of the logits hidden @ weight.T (+ bias) against target.
 
     hidden [N,D] and weight [V,D] are CUDA bf16; target [N] is int64; bias is
     an optional CUDA fp32 [V]. reduction is "mean" (over non-ignored rows,
     the count clamped to one), "sum" or "none" (a loss per row, 0 on ignored
     rows). With filter_eps > 0 the backward leaves out 128x256 gradient tiles
-    whose every |softmax - onehot| is below it.
+    whose every |softmax - onehot| is below it; sort_vocab = True makes the
+    backward visit the vocabulary by decreasing average logit, which groups
+    the negligible columns into tiles the filter can leave out (Cut
+    Cross-Entropy, Sec. 4.3 "Vocabulary sorting").
     """
     if reduction not in B.REDUCTIONS:
         raise ValueError(f"reduction must be one of {sorted(B.REDUCTIONS)}")
-    loss, lse = _LinearCrossEntropy.apply(hidden, weight, bias, target, ignore_index, reduction, filter_eps)
+    flags = B.FLAG_SORT_VOCAB if sort_vocab else 0
+    loss, lse = _LinearCrossEntropy.apply(hidden, weight, bias, target, ignore_index, reduction, filter_eps, flags)
     return (loss, lse) if return_lse else loss
 
 
@@ -95,12 +99,14 @@ class FusedLinearCrossEntropy(torch.nn.Module):
     bias) are passed in, so a tied embedding or an existing lm_head keeps its
     parameter."""
 
-    def __init__(self, ignore_index: int = -100, reduction: str = "mean", filter_eps: float = 0.0):
+    def __init__(self, ignore_index: int = -100, reduction: str = "mean", filter_eps: float = 0.0,
+                 sort_vocab: bool = False):
         super().__init__()
         if reduction not in B.REDUCTIONS:
             raise ValueError(f"reduction must be one of {sorted(B.REDUCTIONS)}")
         self.ignore_index, self.reduction, self.filter_eps = ignore_index, reduction, filter_eps
+        self.sort_vocab = sort_vocab
 
     def forward(self, hidden, weight, target, bias=None):
         return linear_cross_entropy(hidden, weight, target, bias, self.ignore_index, self.reduction,
-                                    self.filter_eps)
+                                    self.filter_eps, sort_vocab=self.sort_vocab)

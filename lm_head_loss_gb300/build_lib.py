@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(LIB_DIR, "libflce.so")
 SOURCES = [os.path.join(CSRC, "flce.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "tile_gemm.cuh"), os.path.join(CSRC, "tile_gemm_pair.cuh"),
                      os.path.join(CSRC, "ptx_sm103.cuh"),
+                     os.path.join(CSRC, "vocab_sort.cuh"),
                      os.path.join(INCLUDE, "flce.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -30,6 +30,7 @@
 #include "flce.h"
 #include "tile_gemm.cuh"
 #include "tile_gemm_pair.cuh"
+#include "vocab_sort.cuh"
 
 namespace flce {
 
@@ -179,12 +180,14 @@ __global__ void set_scale_kernel(const float* __restrict__ grad, int reduction, 
   }
 }
 
-// d(bias) of one staging chunk: out[c] (=|+=) scale * sum over the chunk's
-// rows of G[r][c]. A block covers 32 columns; thread (c, g) sums rows g,
-// g + 8, ... and the 8 partial sums are added in g order (fixed order).
+// d(bias) of one staging chunk: out[dst(c)] (=|+=) scale * sum over the
+// chunk's rows of G[r][c], with dst(c) = v0 + c, or col_map[v0 + c] when the
+// vocabulary runs in sorted order. A block covers 32 columns; thread (c, g)
+// sums rows g, g + 8, ... and the 8 partial sums are added in g order.
 __global__ void __launch_bounds__(256) dbias_chunk_kernel(const __nv_bfloat16* __restrict__ stage, int ld, int rows,
                                                           int cols, const float* __restrict__ scale,
-                                                          float* __restrict__ out, int accumulate) {
+                                                          float* __restrict__ out, int64_t v0,
+                                                          const int32_t* __restrict__ col_map, int accumulate) {
   __shared__ float part[8][32];
   const int c = blockIdx.x * 32 + threadIdx.x, g = threadIdx.y;
   float acc = 0.f;
@@ -196,7 +199,8 @@ __global__ void __launch_bounds__(256) dbias_chunk_kernel(const __nv_bfloat16* _
     float t = 0.f;
     for (int k = 0; k < 8; ++k) t += part[k][threadIdx.x];
     t *= __ldg(scale);
-    out[c] = accumulate ? out[c] + t : t;
+    const int64_t dst = col_map ? (int64_t)__ldg(col_map + v0 + c) : v0 + c;
+    out[dst] = accumulate ? out[dst] + t : t;
   }
 }
 
@@ -321,6 +325,8 @@ struct Plan {
   int n_vtiles;          // ceil(V / 256)
   int row_chunks, v_chunks;
   size_t off_pm, off_ps, off_zy, off_lse, off_bsum, off_flags[2], off_stage[2];
+  // vocabulary sorting (FLCE_FLAG_SORT_VOCAB only)
+  size_t off_hpart, off_hmean, off_avg, off_keys[2], off_ids[2], off_inv, off_bias_s, off_ys, off_wsort;
   // ignored-row compaction (FLCE_FLAG_COMPACT_IGNORED only)
   size_t off_cidx, off_cpos, off_hc, off_dhc, off_yc, off_lsec, off_rsc;
   size_t total;
@@ -356,6 +362,31 @@ static Plan make_plan_rows(const flce_problem& p, int nc) {
   for (int b = 0; b < 2; ++b) {
     pl.off_stage[b] = off;
     off = align_up(off + (size_t)pl.nc * pl.vc * 2, 1024);
+  }
+  if (p.flags & FLCE_FLAG_SORT_VOCAB) {
+    // Sizes grow with N and V only, so the plan of a compacted problem (fewer
+    // rows, no sort region) ends before this region starts.
+    const size_t n = (size_t)std::max<int64_t>(p.n_rows, 1), d = (size_t)p.hidden, v = (size_t)p.vocab;
+    pl.off_hpart = off;
+    off = align_up(off + (size_t)kHsumMaxSplits * d * 4, 1024);
+    pl.off_hmean = off;
+    off = align_up(off + d * 4, 1024);
+    pl.off_avg = off;
+    off = align_up(off + v * 4, 1024);
+    for (int b = 0; b < 2; ++b) {
+      pl.off_keys[b] = off;
+      off = align_up(off + v * 4, 1024);
+      pl.off_ids[b] = off;
+      off = align_up(off + v * 4, 1024);
+    }
+    pl.off_inv = off;
+    off = align_up(off + v * 4, 1024);
+    pl.off_bias_s = off;
+    off = align_up(off + v * 4, 1024);
+    pl.off_ys = off;
+    off = align_up(off + n * 8, 1024);
+    pl.off_wsort = off;
+    off = align_up(off + v * d * 2, 1024);
   }
   if (p.flags & FLCE_FLAG_COMPACT_IGNORED) {
     const size_t n = (size_t)std::max<int64_t>(p.n_rows, 1), d = (size_t)p.hidden;
@@ -461,7 +492,7 @@ static bool problem_ok(const flce_problem* p) {
   if (p->vocab < 1 || p->vocab >= (int64_t)1 << 31) return false;
   if (!(p->filter_eps >= 0.f) || !std::isfinite(p->filter_eps)) return false;
   if ((p->flags & ~(FLCE_FLAG_TEST_SHORT_WAITS | FLCE_FLAG_FILTER_FULL_DW | FLCE_FLAG_FILTER_FULL_DH |
-                    FLCE_FLAG_COMPACT_IGNORED)) != 0u)
+                    FLCE_FLAG_COMPACT_IGNORED | FLCE_FLAG_SORT_VOCAB)) != 0u)
     return false;
   return true;
 }
@@ -691,9 +722,13 @@ static flce_status run_forward(const flce_problem& p, const Plan& pl, const Maps
 // The backward walks (row chunk, vocabulary chunk) items in order. Item s
 // stages its dZ in buffer s % 2. The dZ GEMM of item s+1 shares a launch with
 // the dW and dH GEMMs of item s: they touch different staging buffers.
+// vocab_map (sorted vocabulary only): vocabulary position i of this problem
+// is id vocab_map[i]; dW rows and d(bias) entries are written to their ids
+// in dW_out / dbias, so mp.dw is not used.
 static flce_status run_backward(const flce_problem& p, const Plan& pl, const Maps& mp, const int64_t* y,
                                 const float* lse, uint8_t* ws, int sms, cudaStream_t st, const float* bias = nullptr,
-                                const float* row_scale = nullptr, float* dbias = nullptr) {
+                                const float* row_scale = nullptr, float* dbias = nullptr,
+                                const int32_t* vocab_map = nullptr, float* dW_out = nullptr) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int filter = p.filter_eps > 0.f ? 1 : 0;
   const int d_tiles = (int)ceil_div(p.hidden, kBN);
@@ -741,7 +776,7 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     const __nv_bfloat16* stage = reinterpret_cast<const __nv_bfloat16*>(ws + pl.off_stage[s & 1]);
     ProfScope prof(FLCE_KERNEL_DBIAS, st);
     dbias_chunk_kernel<<<(int)ceil_div(cols, 32), dim3(32, 8), 0, st>>>(stage, pl.vcu, rows, cols, &hdr->scale,
-                                                                        dbias + v0, rc > 0 ? 1 : 0);
+                                                                        dbias, v0, vocab_map, rc > 0 ? 1 : 0);
     return cudaGetLastError() == cudaSuccess;
   };
   auto count_skipped = [&](const GemmParams& dz) -> bool {
@@ -785,6 +820,14 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     dw.flags = flags;
     dw.flags_ld = pl.vcu / kBN;
     dw.flags_a_is_rows = 0;
+    if (vocab_map) {
+      dw.m_valid = cols;
+      dw.out_rows = vocab_map;
+      dw.out_ptr = dW_out;
+      dw.out_ld = p.hidden;
+      dw.out_cols = (int32_t)p.hidden;
+      dw.out_rows_n = (int32_t)p.vocab;
+    }
     g.add(mp.s_mn[b], mp.h_mn, mp.dw, dw);
     // dH[r0 : r0+rows, :] (=|+=) scale * staging * W[v0 : v0+cols, :]
     GemmParams dh = base_params(p, hdr);
@@ -854,12 +897,89 @@ static bool build_maps(const flce_problem& p, const Plan& pl, const void* H, con
   return true;
 }
 
+// Vocabulary sorting (FLCE_FLAG_SORT_VOCAB, Cut Cross-Entropy Sec. 4.3):
+// average logit of every id over the valid rows, their stable descending
+// order, W, the bias and the targets rearranged in that order, then the
+// backward of the rearranged problem, which writes dW and d(bias) back in id
+// order. `sp` is the plan that holds the sort buffers: the caller's full
+// plan, also when the rows were compacted into `p` (whose own plan `pl` has
+// no sort region and ends before it).
+static flce_status run_backward_sorted(const flce_problem& p, const Plan& pl, const Plan& sp, const Maps& mp,
+                                       const void* H, const void* W, const int64_t* y, const float* lse, float* dW,
+                                       uint8_t* ws, int sms, cudaStream_t st, const float* bias,
+                                       const float* row_scale, float* dbias) {
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
+  const int d = (int)p.hidden;
+  const int64_t n = p.n_rows, v = p.vocab;
+  float* hpart = reinterpret_cast<float*>(ws + sp.off_hpart);
+  float* hmean = reinterpret_cast<float*>(ws + sp.off_hmean);
+  float* avg = reinterpret_cast<float*>(ws + sp.off_avg);
+  uint32_t* keys0 = reinterpret_cast<uint32_t*>(ws + sp.off_keys[0]);
+  uint32_t* keys1 = reinterpret_cast<uint32_t*>(ws + sp.off_keys[1]);
+  int32_t* order = reinterpret_cast<int32_t*>(ws + sp.off_ids[0]);
+  int32_t* ids1 = reinterpret_cast<int32_t*>(ws + sp.off_ids[1]);
+  int32_t* inv = reinterpret_cast<int32_t*>(ws + sp.off_inv);
+  float* bias_s = bias ? reinterpret_cast<float*>(ws + sp.off_bias_s) : nullptr;
+  int64_t* ys = reinterpret_cast<int64_t*>(ws + sp.off_ys);
+  void* w_sorted = ws + sp.off_wsort;
+  const int splits = hsum_splits(n);
+  const unsigned vocab_blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * 8, ceil_div(v, 8)));
+  {
+    ProfScope prof(FLCE_KERNEL_VOCAB_KEYS, st);
+    hsum_partial_kernel<<<dim3((unsigned)ceil_div(d, kHsumCols), (unsigned)splits), 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(H), n, d, y, v, p.ignore_index, splits, hpart);
+    if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+  {
+    ProfScope prof(FLCE_KERNEL_VOCAB_KEYS, st);
+    hmean_kernel<<<(unsigned)ceil_div(d, 256), 256, 0, st>>>(hpart, splits, d, &hdr->count, hmean);
+    if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+  {
+    ProfScope prof(FLCE_KERNEL_VOCAB_KEYS, st);
+    avg_logit_kernel<<<vocab_blocks, kVocabWarpsPerBlock * 32, 0, st>>>(static_cast<const __nv_bfloat16*>(W), v, d,
+                                                                        hmean, bias, avg, keys0);
+    if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+  {
+    ProfScope prof(FLCE_KERNEL_VOCAB_SORT, st);
+    radix_sort_kernel<<<1, kSortThreads, 0, st>>>(keys0, keys1, order, ids1, inv, (int)v);
+    if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+  {
+    ProfScope prof(FLCE_KERNEL_VOCAB_GATHER, st);
+    gather_vocab_kernel<<<vocab_blocks, kVocabWarpsPerBlock * 32, 0, st>>>(
+        static_cast<const uint4*>(W), d / 8, order, v, static_cast<uint4*>(w_sorted), bias, bias_s);
+    if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+  {
+    ProfScope prof(FLCE_KERNEL_VOCAB_GATHER, st);
+    remap_targets_kernel<<<(unsigned)ceil_div(n, 256), 256, 0, st>>>(y, n, v, p.ignore_index, inv, ys);
+    if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+  Maps ms = mp;
+  const uint64_t D = (uint64_t)d, V = (uint64_t)v;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&ms.w_k, bf, w_sorted, D, V, D * 2, 64, kBN)) return FLCE_ERR_CUDA;
+  if (!make_map(&ms.w_k_half, bf, w_sorted, D, V, D * 2, 64, kBN / 2)) return FLCE_ERR_CUDA;
+  if (!make_map(&ms.w_mn, bf, w_sorted, D, V, D * 2, 64, 64)) return FLCE_ERR_CUDA;
+  // Ignored rows carry target -1 in the sorted problem: a valid sorted
+  // position can equal the caller's ignore index when that lies in [0, V).
+  flce_problem ps = p;
+  ps.ignore_index = -1;
+  return run_backward(ps, pl, ms, ys, lse, ws, sms, st, bias_s, row_scale, dbias, order, dW);
+}
+
 static flce_status run_backward_any(const flce_problem& p, const Plan& pl, const Maps& mp, const void* H,
                                     const void* W, const int64_t* y, const float* lse, float* dH, float* dW,
                                     uint8_t* ws, int sms, cudaStream_t st, const float* bias, const float* row_scale,
                                     float* dbias) {
-  if (!(p.flags & FLCE_FLAG_COMPACT_IGNORED))
-    return run_backward(p, pl, mp, y, lse, ws, sms, st, bias, row_scale, dbias);
+  const bool sorted = (p.flags & FLCE_FLAG_SORT_VOCAB) != 0u;
+  auto plain = [&]() {
+    return sorted ? run_backward_sorted(p, pl, pl, mp, H, W, y, lse, dW, ws, sms, st, bias, row_scale, dbias)
+                  : run_backward(p, pl, mp, y, lse, ws, sms, st, bias, row_scale, dbias);
+  };
+  if (!(p.flags & FLCE_FLAG_COMPACT_IGNORED)) return plain();
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   int32_t* idx = reinterpret_cast<int32_t*>(ws + pl.off_cidx);
   int32_t* pos = reinterpret_cast<int32_t*>(ws + pl.off_cpos);
@@ -869,7 +989,7 @@ static flce_status run_backward_any(const flce_problem& p, const Plan& pl, const
   int64_t count = 0;
   if (cudaStreamSynchronize(st) != cudaSuccess) return FLCE_ERR_CUDA;
   if (cudaMemcpy(&count, &hdr->count, sizeof(count), cudaMemcpyDeviceToHost) != cudaSuccess) return FLCE_ERR_CUDA;
-  if (count == p.n_rows) return run_backward(p, pl, mp, y, lse, ws, sms, st, bias, row_scale, dbias);
+  if (count == p.n_rows) return plain();
   if (count == 0) {
     if (cudaMemsetAsync(dH, 0, (size_t)p.n_rows * p.hidden * 4, st) != cudaSuccess) return FLCE_ERR_CUDA;
     if (cudaMemsetAsync(dW, 0, (size_t)p.vocab * p.hidden * 4, st) != cudaSuccess) return FLCE_ERR_CUDA;
@@ -886,12 +1006,14 @@ static flce_status run_backward_any(const flce_problem& p, const Plan& pl, const
   if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
   flce_problem pc = p;
   pc.n_rows = count;
-  pc.flags &= ~FLCE_FLAG_COMPACT_IGNORED;
-  Plan plc = make_plan(pc);   // fits in front of the compaction buffers: plc.total <= pl.off_cidx
+  pc.flags &= ~(FLCE_FLAG_COMPACT_IGNORED | FLCE_FLAG_SORT_VOCAB);
+  // Fits in front of the sort and compaction buffers of the full plan.
+  Plan plc = make_plan(pc);
   choose_backward_chunk(plc, pc, sms);
   Maps mpc;
   if (!build_maps(pc, plc, Hc, W, dHc, dW, ws, true, &mpc)) return FLCE_ERR_CUDA;
-  flce_status r = run_backward(pc, plc, mpc, yc, lsec, ws, sms, st, bias, rsc, dbias);
+  flce_status r = sorted ? run_backward_sorted(pc, plc, pl, mpc, Hc, W, yc, lsec, dW, ws, sms, st, bias, rsc, dbias)
+                         : run_backward(pc, plc, mpc, yc, lsec, ws, sms, st, bias, rsc, dbias);
   if (r != FLCE_OK) return r;
   scatter_rows_kernel<<<(unsigned)p.n_rows, 256, 0, st>>>(reinterpret_cast<const float4*>(dHc), (int)(p.hidden / 4),
                                                           pos, reinterpret_cast<float4*>(dH));
@@ -1074,6 +1196,23 @@ flce_status flce_backward_ex(const flce_problem* p, int32_t reduction, const voi
   if (!build_maps(*p, pl, H, W, dH, dW, wsb, true, &mp)) return FLCE_ERR_CUDA;
   return run_backward_any(*p, pl, mp, H, W, y, lse, dH, dW, wsb, sms, st, bias,
                           reduction == FLCE_REDUCTION_NONE ? grad : nullptr, dbias);
+}
+
+flce_status flce_get_vocab_order(const flce_problem* p, const void* ws, int32_t* order, float* avg_logit,
+                                 void* stream) {
+  if (!problem_ok(p) || !(p->flags & FLCE_FLAG_SORT_VOCAB)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!ws || !aligned(ws, 256) || !order || !aligned(order, 4)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (avg_logit && !aligned(avg_logit, 4)) return FLCE_ERR_INVALID_ARGUMENT;
+  const Plan pl = make_plan(*p);
+  const uint8_t* wsb = static_cast<const uint8_t*>(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = (size_t)p->vocab * 4;
+  if (cudaMemcpyAsync(order, wsb + pl.off_ids[0], bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  if (avg_logit &&
+      cudaMemcpyAsync(avg_logit, wsb + pl.off_avg, bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  return FLCE_OK;
 }
 
 flce_status flce_get_device_status(void* ws, void* stream) {

@@ -88,6 +88,15 @@ struct GemmParams {
   uint32_t* flags;             // per staging tile: 4 quarter flags packed in one word
   int32_t flags_ld;            // staging tiles per staging row-tile
   int32_t flags_a_is_rows;     // REDUCE/STORE skip lookup: 1 = K indexes staging columns (dH)
+  // STORE / REDUCE with a row map: local row r is written to row
+  // out_rows[out_m0 + r] of out_ptr (leading dimension out_ld, out_cols
+  // columns) by plain stores or vector reductions instead of TMA; rows with
+  // out_m0 + r >= out_rows_n or r >= m_valid are padding.
+  const int32_t* out_rows;
+  float* out_ptr;
+  int64_t out_ld;
+  int32_t out_cols;
+  int32_t out_rows_n;
   uint32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -346,7 +355,43 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
       for (int kb = 0; kb < p.k_blocks && all_skipped; ++kb) all_skipped = kblock_skipped_n(p, mt_first, group, kb);
     }
     const float sc = __ldg(p.scale);
-    if (!(all_skipped && p.mode == EPI_REDUCE)) {
+    if (p.out_rows) {
+      // Row-mapped output (a vocabulary visited in sorted order writes dW
+      // rows back in id order): one thread per row, 128 contiguous bytes
+      // per 32-column slice. The map is a permutation of the output rows.
+      const int srow = p.out_m0 + lrow;
+      const bool row_ok = lrow < p.m_valid && srow < p.out_rows_n;
+      float* orow = p.out_ptr + (row_ok ? (int64_t)__ldg(p.out_rows + srow) * p.out_ld : 0);
+      if (!(all_skipped && p.mode == EPI_REDUCE)) {
+#pragma unroll 1
+        for (int c = 0; c < kBN; c += 32) {
+          float x[32];
+          if (all_skipped) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = 0.f;
+          } else {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(taddr + c, r);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * sc;
+          }
+          const int col = nt * kBN + c;
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              const int cc = col + 4 * v;
+              if (cc < p.out_cols) {
+                if (p.mode == EPI_REDUCE)
+                  ptx::red_add_v4(orow + cc, x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
+                else
+                  *reinterpret_cast<float4*>(orow + cc) = make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
+              }
+            }
+          }
+        }
+      }
+    } else if (!(all_skipped && p.mode == EPI_REDUCE)) {
 #pragma unroll 1
       for (int c = 0; c < kBN; c += 32) {
         uint8_t* sbox = my_boxes + ebuf * kEpiBoxBytes;

@@ -92,11 +92,13 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return bf16_bits_to_f32(bits).astype(np.float64)
 
 
-def normal_bf16(seed: int, shape: tuple[int, ...], std: float) -> np.ndarray:
+def normal_bf16(seed: int, shape: tuple[int, ...], std: float, shift: np.ndarray | None = None) -> np.ndarray:
     """N(0, std^2) samples as bf16 bit patterns (uint16), Box-Muller in fp64.
 
     Pair k uses uniforms u1 = U[2k], u2 = U[2k+1]; r = sqrt(-2 ln(1 - u1));
     element 2k = r cos(2 pi u2) * std, element 2k+1 = r sin(2 pi u2) * std.
+    shift (fp64, one value per index of the last axis) is added to every
+    row before the single rounding to bf16.
     """
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.uint16)
@@ -111,6 +113,8 @@ def normal_bf16(seed: int, shape: tuple[int, ...], std: float) -> np.ndarray:
         z[1::2] = r * np.sin(t)
         z *= std
         e0, e1 = 2 * p0, min(n, 2 * p1)
+        if shift is not None:
+            z[: e1 - e0] += shift[np.arange(e0, e1) % shape[-1]]
         out[e0:e1] = f64_to_bf16_bits(z[: e1 - e0])
     return out.reshape(shape)
 
@@ -188,6 +192,10 @@ class Workload:
     ignore_frac: float
     zipf_s: float = 1.1
     description: str = ""
+    # H_n = N(0, I) + h_shared * sqrt(D) * u for one seeded unit vector u:
+    # a component every row shares, which gives each token a logit offset
+    # W_v . u common to all rows (a frequency prior of the vocabulary).
+    h_shared: float = 0.0
 
     @property
     def w_std(self) -> float:
@@ -224,12 +232,21 @@ WORKLOADS: dict[str, Workload] = {
                                                    "for profiler captures (about 1.3 GB on the device)"),
     "long128k_head": Workload("long128k_head", 131072, 2048, 151552, 1.0, "zipf", 0.10,
                               description="Gravity-16B-A3B head at 128K context"),
+    "gemma2_2b_head_prior": Workload("gemma2_2b_head_prior", 8192, 2304, 256000, 9.0, "top16", 0.0,
+                                     description="Gemma-2-2B-shaped head whose rows share a component, "
+                                                 "so tokens carry a common logit prior", h_shared=2.0),
 }
 
 
 def make_inputs(wl: Workload, seed: int = 0) -> dict:
     """H [N,D] and W [V,D] as bf16 bit patterns (uint16) and y [N] int64."""
-    h = normal_bf16(_subseed(seed, "H"), (wl.n_rows, wl.hidden), 1.0)
+    shift = None
+    if wl.h_shared != 0.0:
+        u = np.array([0.0])
+        while not np.linalg.norm(u) > 0.0:
+            u = bf16_bits_to_f64(normal_bf16(_subseed(seed, "Hshared"), (wl.hidden,), 1.0))
+        shift = u * (wl.h_shared * math.sqrt(wl.hidden) / np.linalg.norm(u))
+    h = normal_bf16(_subseed(seed, "H"), (wl.n_rows, wl.hidden), 1.0, shift)
     w = normal_bf16(_subseed(seed, "W"), (wl.vocab, wl.hidden), wl.w_std)
     if wl.targets == "uniform":
         y = uniform_targets(_subseed(seed, "y"), wl.n_rows, wl.vocab)

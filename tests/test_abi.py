@@ -20,7 +20,8 @@ def test_library_exports_every_declared_symbol():
     assert set(declared) == {"flce_workspace_bytes", "flce_forward", "flce_forward_backward",
                              "flce_get_device_status", "flce_status_string", "flce_get_filter_stats",
                              "flce_profile_set", "flce_profile_count", "flce_forward_static_scratch",
-                             "flce_forward_ex", "flce_backward_ex", "flce_forward_workspace_bytes"}
+                             "flce_forward_ex", "flce_backward_ex", "flce_forward_workspace_bytes",
+                             "flce_get_vocab_order"}
     out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
     for name in declared:
@@ -67,6 +68,27 @@ def test_forward_workspace_is_the_front_of_the_full_one():
     assert flce.flce_forward_workspace_bytes(None) == 0
 
 
+def test_sorted_vocabulary_workspace_and_getter_checks():
+    base = flce.make_problem(8192, 2048, 151552)
+    srt = flce.make_problem(8192, 2048, 151552, flags=flce.FLAG_SORT_VOCAB)
+    grow = flce.flce_workspace_bytes(srt) - flce.flce_workspace_bytes(base)
+    v, d, n = 151552, 2048, 8192
+    assert v * d * 2 <= grow <= v * d * 2 + 28 * v + 8 * n + 1028 * d + 12 * 1024
+    # The forward needs none of it.
+    assert flce.flce_forward_workspace_bytes(srt) == flce.flce_forward_workspace_bytes(base)
+    # Sorting and compaction together: the compaction buffers come after.
+    both = flce.make_problem(8192, 2048, 151552, flags=flce.FLAG_SORT_VOCAB | flce.FLAG_COMPACT_IGNORED)
+    comp = flce.make_problem(8192, 2048, 151552, flags=flce.FLAG_COMPACT_IGNORED)
+    assert flce.flce_workspace_bytes(both) - flce.flce_workspace_bytes(comp) == grow
+    st = flce.flce_get_vocab_order
+    assert st(base, FAKE, FAKE, None, 0) == Status.ERR_INVALID_ARGUMENT      # flag not set
+    assert st(srt, None, FAKE, None, 0) == Status.ERR_INVALID_ARGUMENT
+    assert st(srt, FAKE, None, None, 0) == Status.ERR_INVALID_ARGUMENT
+    assert st(srt, FAKE + 16, FAKE, None, 0) == Status.ERR_INVALID_ARGUMENT
+    assert st(srt, FAKE, FAKE + 2, None, 0) == Status.ERR_INVALID_ARGUMENT
+    assert st(None, FAKE, FAKE, None, 0) == Status.ERR_INVALID_ARGUMENT
+
+
 def test_workspace_bytes_rejects_bad_problems():
     assert flce.flce_workspace_bytes(None) == 0
     for args in [(-1, 8, 10), (4, 0, 10), (4, 8, 0), (4, 8, 1 << 31)]:
@@ -74,6 +96,7 @@ def test_workspace_bytes_rejects_bad_problems():
     assert flce.flce_workspace_bytes(flce.make_problem(4, 8, 10, filter_eps=-1.0)) == 0
     assert flce.flce_workspace_bytes(flce.make_problem(4, 8, 10, filter_eps=math.inf)) == 0
     assert flce.flce_workspace_bytes(flce.make_problem(4, 8, 10, flags=0x80)) == 0
+    assert flce.flce_workspace_bytes(flce.make_problem(4, 8, 10, flags=0x20)) == 0
     assert flce.flce_workspace_bytes(flce.make_problem(0, 8, 10)) > 0
 
 
@@ -101,7 +124,7 @@ def test_host_argument_checks_return_before_any_launch():
     assert _fwd(good, H=FAKE + 8) == Status.ERR_UNSUPPORTED                 # TMA needs 16-byte alignment
     assert _fwd(good, nb=flce.flce_forward_workspace_bytes(good) - 1) == Status.ERR_WORKSPACE_TOO_SMALL
     assert _fwd(flce.make_problem(16, 60, 100)) == Status.ERR_UNSUPPORTED   # D % 8 != 0
-    assert _fwd(flce.make_problem(16, 64, 100, flags=0x10)) == Status.ERR_INVALID_ARGUMENT
+    assert _fwd(flce.make_problem(16, 64, 100, flags=0x20)) == Status.ERR_INVALID_ARGUMENT
     assert _fwd(flce.make_problem(16, 64, 100, filter_eps=float("nan"))) == Status.ERR_INVALID_ARGUMENT
     assert _fb(good, dW=None) == Status.ERR_INVALID_ARGUMENT
     assert _fb(good, dH=None) == Status.ERR_INVALID_ARGUMENT

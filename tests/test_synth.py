@@ -111,3 +111,20 @@ def test_page_memory_figures():
     assert round(w128.logits_bytes_bf16() / 2 ** 30, 2) == f["value"]
     f = by_id["gemma2_2b_gradient_lower_bound"]
     assert round(wl["gemma2_2b_head"].grad_bytes_bf16() / 2 ** 20) == f["value"]
+
+
+def test_shared_component_workload():
+    base = synth.Workload("b", 600, 64, 100, 1.0, "uniform", 0.0)
+    shared = synth.Workload("s", 600, 64, 100, 1.0, "uniform", 0.0, h_shared=2.0)
+    a = synth.make_inputs(base, seed=4)
+    b = synth.make_inputs(shared, seed=4)
+    # W and y come from their own streams; without a shared component H is unchanged.
+    assert np.array_equal(a["W"], b["W"]) and np.array_equal(a["y"], b["y"])
+    assert np.array_equal(synth.make_inputs(base, seed=4)["H"], a["H"])
+    ha = synth.bf16_bits_to_f64(a["H"])
+    hb = synth.bf16_bits_to_f64(b["H"])
+    shift = hb.mean(axis=0) - ha.mean(axis=0)
+    # The shift has norm h_shared * sqrt(D); the two means differ only by it
+    # (up to one bf16 rounding per element).
+    assert abs(np.linalg.norm(shift) - 2.0 * math.sqrt(64)) < 0.1
+    assert np.max(np.abs((hb - ha) - shift[None, :])) < 2.0 ** -6 * (np.max(np.abs(hb)) + 1)
