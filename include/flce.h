@@ -112,7 +112,7 @@ typedef struct {
  *   W_v . mean(H over valid rows) (+ b_v), the same value by linearity,
  *   in fp32; ids of equal average keep their id order.
  *   The backward runs on a copy of W with its rows in that order (kept in
- *   the workspace, which grows by V*D*2 + 28*V + 8*N + 1028*D bytes) and
+ *   the workspace, which grows by at most V*D*2 + 29*V + 8*N + 1028*D bytes) and
  *   writes dW and d(bias) back to the caller's buffers in id order. With
  *   filtering off the results equal those of the unsorted backward up to
  *   fp32 summation order. The forward ignores the flag.
@@ -184,6 +184,43 @@ flce_status flce_backward_ex(const flce_problem* p, int32_t reduction, const voi
  * first in that order that is set wins, timeout over bad target) and clears it. */
 flce_status flce_get_device_status(void* ws, void* stream);
 
+/* Hyper-parameters of one AdamW step (decoupled weight decay, bias-corrected
+ * moments, the form torch.optim.AdamW computes), read by the kernels from
+ * device memory so that a captured CUDA graph picks up each step's values. */
+typedef struct {
+  float lr;
+  float beta1;         /* in [0, 1) */
+  float beta2;         /* in [0, 1) */
+  float eps;           /* > 0 */
+  float weight_decay;
+  int32_t step;        /* t >= 1: the step being taken (bias corrections 1 - beta^t) */
+} flce_adamw_hparams;
+
+/* flce_forward_backward with W's AdamW update fused into its gradient, as
+ * the FORGE explainer describes ("FORGE: Fused On-Register Gradient
+ * Elimination for Memory-Efficient LLM Training", Sec. 2): each finished
+ * dW tile, still in the tensor cores' accumulator, updates its rows of the
+ * fp32 master weights and moments, writes their bf16 copy, and is dropped.
+ * dW never reaches memory.
+ *   w_master, adam_m, adam_v: device fp32 [V,D], read and updated in place.
+ *   w_out: device bf16 [V,D], receives the updated weights rounded to
+ *     nearest; it must not overlap W, which the same call still reads.
+ *   hp: device pointer to this step's hyper-parameters. A step below 1, a
+ *     beta outside [0, 1), eps <= 0 or a non-finite lr / weight_decay leave
+ *     the master weights and moments unchanged and make
+ *     flce_get_device_status report FLCE_ERR_INVALID_ARGUMENT.
+ *   Other arguments and results as flce_forward_backward (dH, LSE, loss).
+ *   The rows must fit one 8192-row chunk (n_rows in 1..8192), so each dW
+ *   tile is complete after one contraction; otherwise FLCE_ERR_UNSUPPORTED.
+ *   The gradient of a tile is final only when the whole batch is in it: a
+ *   data-parallel run that must all-reduce dW cannot use this entry point
+ *   (the page says the same of FORGE). Combines with filtering, sorting and
+ *   ignored-row compaction. Workspace: flce_workspace_bytes(p). */
+flce_status flce_forward_backward_adamw(const flce_problem* p, const void* H, const void* W, const int64_t* y,
+                                        float grad_loss, float* lse, float* loss, float* dH, float* w_master,
+                                        float* adam_m, float* adam_v, void* w_out, const flce_adamw_hparams* hp,
+                                        void* ws, size_t ws_bytes, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* flce_status_string(flce_status s);
 
@@ -250,6 +287,7 @@ flce_status flce_forward_static_scratch(const flce_problem* p, const void* H, co
 #define FLCE_KERNEL_VOCAB_KEYS 11   /* average logits: column sums of H, their mean, W . mean */
 #define FLCE_KERNEL_VOCAB_SORT 12   /* stable radix sort of the averages, inverse order */
 #define FLCE_KERNEL_VOCAB_GATHER 13 /* W, bias and targets rearranged in the sorted order */
+#define FLCE_KERNEL_ADAMW_PREP 14   /* constants of the fused AdamW step */
 flce_status flce_profile_set(void** events, int32_t* kinds, int32_t cap);
 int32_t flce_profile_count(void);
 

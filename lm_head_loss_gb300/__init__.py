@@ -12,6 +12,8 @@ from ._binding import (  # noqa: F401
     FLAG_SORT_VOCAB,
     FLAG_TEST_SHORT_WAITS,
     REDUCTIONS,
+    AdamwHparams,
+    adamw_hparams_bytes,
     FlceError,
     FlceProblem,
     LaunchProfiler,
@@ -20,6 +22,7 @@ from ._binding import (  # noqa: F401
     flce_forward,
     flce_backward_ex,
     flce_forward_backward,
+    flce_forward_backward_adamw,
     flce_forward_ex,
     flce_forward_static_scratch,
     flce_forward_workspace_bytes,
@@ -31,5 +34,6 @@ from ._binding import (  # noqa: F401
     lib,
     make_problem,
 )
-from .api import Workspace, device_status, forward, forward_backward  # noqa: F401
+from .api import (FusedAdamWHead, Workspace, adamw_hparams, device_status, forward,  # noqa: F401
+                  forward_backward, forward_backward_adamw)
 from .autograd import FusedLinearCrossEntropy, linear_cross_entropy  # noqa: F401

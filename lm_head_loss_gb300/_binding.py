@@ -53,6 +53,23 @@ class FlceProblem(ctypes.Structure):
     ]
 
 
+class AdamwHparams(ctypes.Structure):
+    """flce_adamw_hparams: one AdamW step's hyper-parameters (kept in device memory)."""
+    _fields_ = [
+        ("lr", ctypes.c_float),
+        ("beta1", ctypes.c_float),
+        ("beta2", ctypes.c_float),
+        ("eps", ctypes.c_float),
+        ("weight_decay", ctypes.c_float),
+        ("step", ctypes.c_int32),
+    ]
+
+
+def adamw_hparams_bytes(lr: float, beta1: float, beta2: float, eps: float, weight_decay: float, step: int) -> bytes:
+    """The struct's bytes, for a caller to copy into device memory."""
+    return bytes(AdamwHparams(lr, beta1, beta2, eps, weight_decay, step))
+
+
 def make_problem(n_rows: int, hidden: int, vocab: int, ignore_index: int = -100,
                  filter_eps: float = 0.0, flags: int = 0) -> FlceProblem:
     return FlceProblem(n_rows, hidden, vocab, ignore_index, filter_eps, flags)
@@ -73,6 +90,8 @@ def _load() -> ctypes.CDLL:
     lib.flce_forward.restype = ctypes.c_int
     lib.flce_forward_backward.argtypes = [prob, vp, vp, vp, f32, vp, vp, vp, vp, vp, sz, vp]
     lib.flce_forward_backward.restype = ctypes.c_int
+    lib.flce_forward_backward_adamw.argtypes = [prob, vp, vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.flce_forward_backward_adamw.restype = ctypes.c_int
     lib.flce_get_device_status.argtypes = [vp, vp]
     lib.flce_get_device_status.restype = ctypes.c_int
     lib.flce_status_string.argtypes = [ctypes.c_int]
@@ -147,6 +166,15 @@ def flce_forward_backward(problem, H, W, y, grad_loss: float, lse, loss, dH, dW,
                                             _addr(dH), _addr(dW), _addr(ws), nb, _stream(stream)))
 
 
+def flce_forward_backward_adamw(problem, H, W, y, grad_loss: float, lse, loss, dH, w_master, adam_m, adam_v, w_out,
+                                hparams, ws, ws_bytes: int | None = None, stream=None) -> Status:
+    nb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    return Status(lib.flce_forward_backward_adamw(
+        ctypes.byref(problem) if problem is not None else None, _addr(H), _addr(W), _addr(y), float(grad_loss),
+        _addr(lse), _addr(loss), _addr(dH), _addr(w_master), _addr(adam_m), _addr(adam_v), _addr(w_out),
+        _addr(hparams), _addr(ws), nb, _stream(stream)))
+
+
 def flce_forward_ex(problem, reduction: int, H, W, bias, y, lse, loss, ws, ws_bytes: int | None = None,
                     stream=None) -> Status:
     nb = _nbytes(ws) if ws_bytes is None else ws_bytes
@@ -196,7 +224,7 @@ def flce_get_vocab_order(problem, ws, order, avg_logit=None, stream=None) -> Sta
 
 KERNEL_KINDS = {0: "gemm_lse", 1: "gemm_dz", 2: "gemm_dw", 3: "gemm_dh", 4: "prep", 5: "combine",
                 6: "finalize", 7: "filter_stats", 8: "gemm_bwd", 9: "dbias", 10: "set_scale",
-                11: "vocab_keys", 12: "vocab_sort", 13: "vocab_gather"}
+                11: "vocab_keys", 12: "vocab_sort", 13: "vocab_gather", 14: "adamw_prep"}
 
 
 class LaunchProfiler:

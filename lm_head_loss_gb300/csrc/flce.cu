@@ -48,7 +48,9 @@ struct alignas(256) WsHeader {
   float loss;
   unsigned long long tiles_total;
   unsigned long long tiles_skipped;
+  float opt[kAdamwConsts];   // fused AdamW step constants (flce_forward_backward_adamw)
 };
+static_assert(sizeof(WsHeader) == 256, "the header occupies the first 256 bytes of the workspace");
 
 // ------------------------------------------------------------------ kernels
 
@@ -180,6 +182,31 @@ __global__ void set_scale_kernel(const float* __restrict__ grad, int reduction, 
   }
 }
 
+// Constants of one fused AdamW step from the caller's device-side
+// hyper-parameters, the bias corrections in fp64. A step below 1, or a beta
+// outside [0, 1), records kDevBadHparams and turns the step into one that
+// leaves the weights unchanged.
+__global__ void adamw_prep_kernel(const flce_adamw_hparams* __restrict__ hp, WsHeader* hdr) {
+  if (threadIdx.x != 0) return;
+  const flce_adamw_hparams h = *hp;
+  const bool ok = h.step >= 1 && h.beta1 >= 0.f && h.beta1 < 1.f && h.beta2 >= 0.f && h.beta2 < 1.f &&
+                  h.eps > 0.f && isfinite(h.lr) && isfinite(h.weight_decay);
+  if (!ok) {
+    atomicOr(&hdr->status, kDevBadHparams);
+    const float keep[kAdamwConsts] = {0.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+    for (int i = 0; i < kAdamwConsts; ++i) hdr->opt[i] = keep[i];
+    return;
+  }
+  const double t = (double)h.step;
+  const double bc1 = 1.0 - pow((double)h.beta1, t), bc2 = 1.0 - pow((double)h.beta2, t);
+  hdr->opt[0] = (float)((double)h.lr / bc1);
+  hdr->opt[1] = (float)(1.0 / sqrt(bc2));
+  hdr->opt[2] = (float)(1.0 - (double)h.lr * (double)h.weight_decay);
+  hdr->opt[3] = h.beta1;
+  hdr->opt[4] = h.beta2;
+  hdr->opt[5] = h.eps;
+}
+
 // d(bias) of one staging chunk: out[dst(c)] (=|+=) scale * sum over the
 // chunk's rows of G[r][c], with dst(c) = v0 + c, or col_map[v0 + c] when the
 // vocabulary runs in sorted order. A block covers 32 columns; thread (c, g)
@@ -204,14 +231,30 @@ __global__ void __launch_bounds__(256) dbias_chunk_kernel(const __nv_bfloat16* _
   }
 }
 
-// Filter statistics of one staging chunk: tiles whose flag word is zero were
-// skipped. The chunk's flags occupy rows [0, rows) x columns [0, cols) of a
-// row-major array with leading dimension ld.
+// Filter statistics and keep masks of one staging chunk. The chunk's flags
+// occupy rows [0, rows) x columns [0, cols) of a row-major array with
+// leading dimension ld; a tile whose flag word is zero was filtered out.
+// row_keep[r] bit j and col_keep[j] bit r are set when tile (r, j) holds
+// gradient (rows <= 64 and cols <= 64 by the workspace plan): the dH and dW
+// contractions read one of these words per output tile.
 __global__ void count_skipped_kernel(const uint32_t* __restrict__ flags, int rows, int cols, int ld,
-                                     WsHeader* hdr) {
+                                     WsHeader* hdr, uint64_t* __restrict__ row_keep,
+                                     uint64_t* __restrict__ col_keep) {
   __shared__ unsigned red[256];
   unsigned c = 0;
   for (int i = threadIdx.x; i < rows * cols; i += 256) c += flags[(size_t)(i / cols) * ld + (i % cols)] == 0u ? 1u : 0u;
+  for (int r = threadIdx.x; r < rows; r += 256) {
+    uint64_t k = 0ull;
+    for (int j = 0; j < cols; ++j)
+      if (flags[(size_t)r * ld + j] != 0u) k |= 1ull << j;
+    row_keep[r] = k;
+  }
+  for (int j = threadIdx.x; j < cols; j += 256) {
+    uint64_t k = 0ull;
+    for (int r = 0; r < rows; ++r)
+      if (flags[(size_t)r * ld + j] != 0u) k |= 1ull << r;
+    col_keep[j] = k;
+  }
   red[threadIdx.x] = c;
   __syncthreads();
   for (int s = 128; s > 0; s >>= 1) {
@@ -324,9 +367,9 @@ struct Plan {
   int vcu;               // vocabulary chunk the backward uses (<= vc)
   int n_vtiles;          // ceil(V / 256)
   int row_chunks, v_chunks;
-  size_t off_pm, off_ps, off_zy, off_lse, off_bsum, off_flags[2], off_stage[2];
+  size_t off_pm, off_ps, off_zy, off_lse, off_bsum, off_flags[2], off_keep[2], off_stage[2];
   // vocabulary sorting (FLCE_FLAG_SORT_VOCAB only)
-  size_t off_hpart, off_hmean, off_avg, off_keys[2], off_ids[2], off_inv, off_bias_s, off_ys, off_wsort;
+  size_t off_hpart, off_hmean, off_avg, off_keys[2], off_ids[2], off_inv, off_hist, off_bias_s, off_ys, off_wsort;
   // ignored-row compaction (FLCE_FLAG_COMPACT_IGNORED only)
   size_t off_cidx, off_cpos, off_hc, off_dhc, off_yc, off_lsec, off_rsc;
   size_t total;
@@ -358,7 +401,11 @@ static Plan make_plan_rows(const flce_problem& p, int nc) {
   for (int b = 0; b < 2; ++b) {
     pl.off_flags[b] = off;
     off = align_up(off + (size_t)(pl.nc / kBM) * (pl.vc / kBN) * 4, 1024);
+    // keep masks: one word per staging row tile, then one per column tile
+    pl.off_keep[b] = off;
+    off = align_up(off + (size_t)(pl.nc / kBM + pl.vc / kBN) * 8, 1024);
   }
+  static_assert(kRowChunk / kBM <= 64 && kVocabChunkMax / kBN <= 64, "a keep mask is one 64-bit word");
   for (int b = 0; b < 2; ++b) {
     pl.off_stage[b] = off;
     off = align_up(off + (size_t)pl.nc * pl.vc * 2, 1024);
@@ -381,6 +428,8 @@ static Plan make_plan_rows(const flce_problem& p, int nc) {
     }
     pl.off_inv = off;
     off = align_up(off + v * 4, 1024);
+    pl.off_hist = off;
+    off = align_up(off + (size_t)256 * ceil_div(p.vocab, kSortTile) * 4, 1024);
     pl.off_bias_s = off;
     off = align_up(off + v * 4, 1024);
     pl.off_ys = off;
@@ -532,6 +581,28 @@ struct DeviceInfo {
   bool ready = false;
 };
 
+// Instances of the pair kernel, smallest epilogue set first; a launch takes
+// the first whose set holds every problem's mode and whose kSkip matches.
+struct PairInstance {
+  void (*fn)(const GemmLaunch);
+  bool skip;
+  int modes;
+  uint32_t smem;
+};
+constexpr int kPairInstances = 5;
+static const PairInstance* pair_instances() {
+  static const PairInstance inst[kPairInstances] = {
+      {flce_gemm_pair_kernel<false, kModesForward>, false, kModesForward, pair_smem_bytes(kModesForward)},
+      {flce_gemm_pair_kernel<false, kModesBackward>, false, kModesBackward, pair_smem_bytes(kModesBackward)},
+      {flce_gemm_pair_kernel<true, kModesBackward>, true, kModesBackward, pair_smem_bytes(kModesBackward)},
+      {flce_gemm_pair_kernel<false, kModesBackwardAdamw>, false, kModesBackwardAdamw,
+       pair_smem_bytes(kModesBackwardAdamw)},
+      {flce_gemm_pair_kernel<true, kModesBackwardAdamw>, true, kModesBackwardAdamw,
+       pair_smem_bytes(kModesBackwardAdamw)},
+  };
+  return inst;
+}
+
 static bool device_setup(int* sms_out) {
   static std::mutex mu;
   static DeviceInfo info[64];
@@ -547,12 +618,11 @@ static bool device_setup(int* sms_out) {
     if (cudaFuncSetAttribute(flce_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kGemmSmemBytes) != cudaSuccess)
       return false;
-    if (cudaFuncSetAttribute(flce_gemm_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kPairSmemBytes) != cudaSuccess)
-      return false;
-    if (cudaFuncSetAttribute(flce_gemm_pair_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kPairSmemBytes) != cudaSuccess)
-      return false;
+    const PairInstance* inst = pair_instances();
+    for (int i = 0; i < kPairInstances; ++i)
+      if (cudaFuncSetAttribute(inst[i].fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)inst[i].smem) !=
+          cudaSuccess)
+        return false;
     info[dev].sms = sms;
     info[dev].ready = true;
   }
@@ -620,6 +690,7 @@ struct Group {
   }
 };
 
+
 static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
   if (g.units <= 0) return true;
   ProfScope prof(kind, st);
@@ -633,7 +704,7 @@ static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = g.mode == GEMM_PAIR ? kPairSmemBytes : kGemmSmemBytes;
+  cfg.dynamicSmemBytes = kGemmSmemBytes;   // the pair instances set their own below
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -644,9 +715,18 @@ static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
   cfg.numAttrs = 1;
   if (g.mode == GEMM_PAIR) {
     bool skip = false;
-    for (int q = 0; q < g.L.n_probs; ++q) skip = skip || g.L.prob[q].skip_by_flags != 0;
-    if (skip) return cudaLaunchKernelEx(&cfg, flce_gemm_pair_kernel<true>, g.L) == cudaSuccess;
-    return cudaLaunchKernelEx(&cfg, flce_gemm_pair_kernel<false>, g.L) == cudaSuccess;
+    int modes = 0;
+    for (int q = 0; q < g.L.n_probs; ++q) {
+      skip = skip || g.L.prob[q].skip_by_flags != 0;
+      modes |= 1 << g.L.prob[q].mode;
+    }
+    const PairInstance* inst = pair_instances();
+    for (int i = 0; i < kPairInstances; ++i) {
+      if (inst[i].skip != skip || (modes & ~inst[i].modes) != 0) continue;
+      cfg.dynamicSmemBytes = inst[i].smem;
+      return cudaLaunchKernelEx(&cfg, inst[i].fn, g.L) == cudaSuccess;
+    }
+    return false;   // no instance carries this set of epilogues
   }
   return cudaLaunchKernelEx(&cfg, flce_gemm_kernel<2>, g.L) == cudaSuccess;
 }
@@ -722,13 +802,23 @@ static flce_status run_forward(const flce_problem& p, const Plan& pl, const Maps
 // The backward walks (row chunk, vocabulary chunk) items in order. Item s
 // stages its dZ in buffer s % 2. The dZ GEMM of item s+1 shares a launch with
 // the dW and dH GEMMs of item s: they touch different staging buffers.
+// Fused AdamW on W (flce_forward_backward_adamw): the dW contraction's
+// epilogue updates these instead of writing dW.
+struct OptTarget {
+  float* master;
+  float* m;
+  float* v;
+  __nv_bfloat16* w_out;
+};
+
 // vocab_map (sorted vocabulary only): vocabulary position i of this problem
 // is id vocab_map[i]; dW rows and d(bias) entries are written to their ids
 // in dW_out / dbias, so mp.dw is not used.
 static flce_status run_backward(const flce_problem& p, const Plan& pl, const Maps& mp, const int64_t* y,
                                 const float* lse, uint8_t* ws, int sms, cudaStream_t st, const float* bias = nullptr,
                                 const float* row_scale = nullptr, float* dbias = nullptr,
-                                const int32_t* vocab_map = nullptr, float* dW_out = nullptr) {
+                                const int32_t* vocab_map = nullptr, float* dW_out = nullptr,
+                                const OptTarget* opt = nullptr) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int filter = p.filter_eps > 0.f ? 1 : 0;
   const int d_tiles = (int)ceil_div(p.hidden, kBN);
@@ -779,10 +869,14 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
                                                                         dbias, v0, vocab_map, rc > 0 ? 1 : 0);
     return cudaGetLastError() == cudaSuccess;
   };
-  auto count_skipped = [&](const GemmParams& dz) -> bool {
+  // Statistics and keep masks of item s's flags (buffer s % 2), before the
+  // contractions of item s read them.
+  auto count_skipped = [&](const GemmParams& dz, int s) -> bool {
     if (!filter) return true;
     ProfScope prof(FLCE_KERNEL_FILTER_STATS, st);
-    count_skipped_kernel<<<1, 256, 0, st>>>(dz.flags, dz.m_tiles, dz.n_tiles, dz.flags_ld, hdr);
+    uint64_t* keep = reinterpret_cast<uint64_t*>(ws + pl.off_keep[s & 1]);
+    count_skipped_kernel<<<1, 256, 0, st>>>(dz.flags, dz.m_tiles, dz.n_tiles, dz.flags_ld, hdr, keep,
+                                            keep + pl.nc / kBM);
     return cudaGetLastError() == cudaSuccess;
   };
 
@@ -793,7 +887,7 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     const GemmParams dz0 = dz_params(0);
     g.add(mp.h_k, w_b, mp.s_store[0], dz0);
     if (!launch_group(FLCE_KERNEL_GEMM_DZ, g, sms, st)) return FLCE_ERR_CUDA;
-    if (!count_skipped(dz0)) return FLCE_ERR_CUDA;
+    if (!count_skipped(dz0, 0)) return FLCE_ERR_CUDA;
     if (!dbias_item(0)) return FLCE_ERR_CUDA;
   }
   for (int s = 0; s < items; ++s) {
@@ -802,7 +896,7 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     int rows, cols;
     item_geom(s, r0, rows, v0, cols);
     const int rc = s / pl.v_chunks, vi = s % pl.v_chunks;
-    uint32_t* flags = reinterpret_cast<uint32_t*>(ws + pl.off_flags[b]);
+    const uint64_t* keep = reinterpret_cast<const uint64_t*>(ws + pl.off_keep[b]);
     Group g(gm);
     // dW[v0 : v0+cols, :] (=|+=) scale * staging^T * H[r0 : r0+rows, :]
     GemmParams dw = base_params(p, hdr);
@@ -817,16 +911,24 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     dw.out_m0 = (int32_t)v0;
     dw.scale = &hdr->scale;
     dw.skip_by_flags = filter && !(p.flags & FLCE_FLAG_FILTER_FULL_DW);
-    dw.flags = flags;
-    dw.flags_ld = pl.vcu / kBN;
     dw.flags_a_is_rows = 0;
-    if (vocab_map) {
+    dw.keep = keep + pl.nc / kBM;
+    if (vocab_map || opt) {
       dw.m_valid = cols;
       dw.out_rows = vocab_map;
       dw.out_ptr = dW_out;
       dw.out_ld = p.hidden;
       dw.out_cols = (int32_t)p.hidden;
       dw.out_rows_n = (int32_t)p.vocab;
+    }
+    if (opt) {
+      // One row chunk: each dW tile is complete after this contraction.
+      dw.mode = EPI_ADAMW;
+      dw.out_ptr = opt->master;
+      dw.opt = hdr->opt;
+      dw.opt_m = opt->m;
+      dw.opt_v = opt->v;
+      dw.opt_w = opt->w_out;
     }
     g.add(mp.s_mn[b], mp.h_mn, mp.dw, dw);
     // dH[r0 : r0+rows, :] (=|+=) scale * staging * W[v0 : v0+cols, :]
@@ -842,9 +944,8 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     dh.out_m0 = (int32_t)r0;
     dh.scale = &hdr->scale;
     dh.skip_by_flags = filter && !(p.flags & FLCE_FLAG_FILTER_FULL_DH);
-    dh.flags = flags;
-    dh.flags_ld = pl.vcu / kBN;
     dh.flags_a_is_rows = 1;
+    dh.keep = keep;
     g.add(mp.s_k[b], mp.w_mn, mp.dh, dh);
     GemmParams dz_next;
     const bool has_next = s + 1 < items;
@@ -863,7 +964,7 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
         if (!launch_group(FLCE_KERNEL_GEMM_DZ, gz, sms, st)) return FLCE_ERR_CUDA;
       }
     }
-    if (has_next && !count_skipped(dz_next)) return FLCE_ERR_CUDA;
+    if (has_next && !count_skipped(dz_next, s + 1)) return FLCE_ERR_CUDA;
     if (has_next && !dbias_item(s + 1)) return FLCE_ERR_CUDA;
   }
   return FLCE_OK;
@@ -873,7 +974,7 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
 static flce_status run_backward_any(const flce_problem& p, const Plan& pl, const Maps& mp, const void* H,
                                     const void* W, const int64_t* y, const float* lse, float* dH, float* dW,
                                     uint8_t* ws, int sms, cudaStream_t st, const float* bias, const float* row_scale,
-                                    float* dbias);
+                                    float* dbias, const OptTarget* opt = nullptr);
 
 static bool build_maps(const flce_problem& p, const Plan& pl, const void* H, const void* W, float* dH, float* dW,
                        uint8_t* ws, bool backward, Maps* mp) {
@@ -893,7 +994,7 @@ static bool build_maps(const flce_problem& p, const Plan& pl, const void* H, con
     if (!make_map(&mp->s_mn[b], bf, stage, vc, nc, vc * 2, 64, 64)) return false;
   }
   if (!make_map(&mp->dh, f32, dH, D, N, D * 4, 32, 32)) return false;
-  if (!make_map(&mp->dw, f32, dW, D, V, D * 4, 32, 32)) return false;
+  if (dW && !make_map(&mp->dw, f32, dW, D, V, D * 4, 32, 32)) return false;
   return true;
 }
 
@@ -907,7 +1008,7 @@ static bool build_maps(const flce_problem& p, const Plan& pl, const void* H, con
 static flce_status run_backward_sorted(const flce_problem& p, const Plan& pl, const Plan& sp, const Maps& mp,
                                        const void* H, const void* W, const int64_t* y, const float* lse, float* dW,
                                        uint8_t* ws, int sms, cudaStream_t st, const float* bias,
-                                       const float* row_scale, float* dbias) {
+                                       const float* row_scale, float* dbias, const OptTarget* opt) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   const int d = (int)p.hidden;
   const int64_t n = p.n_rows, v = p.vocab;
@@ -942,8 +1043,30 @@ static flce_status run_backward_sorted(const flce_problem& p, const Plan& pl, co
     if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
   }
   {
+    uint32_t* hist = reinterpret_cast<uint32_t*>(ws + sp.off_hist);
+    const unsigned tiles = (unsigned)ceil_div(v, kSortTile);
+    uint32_t* keys[2] = {keys0, keys1};
+    int32_t* ids[2] = {order, ids1};
+    for (int pass = 0; pass < 4; ++pass) {
+      const int src = pass & 1, shift = 8 * pass;
+      {
+        ProfScope prof(FLCE_KERNEL_VOCAB_SORT, st);
+        radix_hist_kernel<<<tiles, 256, 0, st>>>(keys[src], (int)v, shift, hist);
+      }
+      {
+        ProfScope prof(FLCE_KERNEL_VOCAB_SORT, st);
+        radix_scan_kernel<<<1, 1024, 0, st>>>(hist, (int)(256 * tiles));
+      }
+      {
+        ProfScope prof(FLCE_KERNEL_VOCAB_SORT, st);
+        radix_scatter_kernel<<<tiles, 256, 0, st>>>(keys[src], pass == 0 ? nullptr : ids[src], (int)v, shift, hist,
+                                                    keys[src ^ 1], ids[src ^ 1]);
+      }
+      if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+    }
+    // Four passes end back in keys0 / order.
     ProfScope prof(FLCE_KERNEL_VOCAB_SORT, st);
-    radix_sort_kernel<<<1, kSortThreads, 0, st>>>(keys0, keys1, order, ids1, inv, (int)v);
+    radix_inverse_kernel<<<(unsigned)ceil_div(v, 256), 256, 0, st>>>(order, (int)v, inv);
     if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
   }
   {
@@ -967,17 +1090,17 @@ static flce_status run_backward_sorted(const flce_problem& p, const Plan& pl, co
   // position can equal the caller's ignore index when that lies in [0, V).
   flce_problem ps = p;
   ps.ignore_index = -1;
-  return run_backward(ps, pl, ms, ys, lse, ws, sms, st, bias_s, row_scale, dbias, order, dW);
+  return run_backward(ps, pl, ms, ys, lse, ws, sms, st, bias_s, row_scale, dbias, order, dW, opt);
 }
 
 static flce_status run_backward_any(const flce_problem& p, const Plan& pl, const Maps& mp, const void* H,
                                     const void* W, const int64_t* y, const float* lse, float* dH, float* dW,
                                     uint8_t* ws, int sms, cudaStream_t st, const float* bias, const float* row_scale,
-                                    float* dbias) {
+                                    float* dbias, const OptTarget* opt) {
   const bool sorted = (p.flags & FLCE_FLAG_SORT_VOCAB) != 0u;
   auto plain = [&]() {
-    return sorted ? run_backward_sorted(p, pl, pl, mp, H, W, y, lse, dW, ws, sms, st, bias, row_scale, dbias)
-                  : run_backward(p, pl, mp, y, lse, ws, sms, st, bias, row_scale, dbias);
+    return sorted ? run_backward_sorted(p, pl, pl, mp, H, W, y, lse, dW, ws, sms, st, bias, row_scale, dbias, opt)
+                  : run_backward(p, pl, mp, y, lse, ws, sms, st, bias, row_scale, dbias, nullptr, nullptr, opt);
   };
   if (!(p.flags & FLCE_FLAG_COMPACT_IGNORED)) return plain();
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
@@ -989,7 +1112,9 @@ static flce_status run_backward_any(const flce_problem& p, const Plan& pl, const
   int64_t count = 0;
   if (cudaStreamSynchronize(st) != cudaSuccess) return FLCE_ERR_CUDA;
   if (cudaMemcpy(&count, &hdr->count, sizeof(count), cudaMemcpyDeviceToHost) != cudaSuccess) return FLCE_ERR_CUDA;
-  if (count == p.n_rows) return plain();
+  // With no valid row the fused optimizer still takes its step (a zero
+  // gradient); the uncompacted backward gives it one.
+  if (count == p.n_rows || (count == 0 && opt)) return plain();
   if (count == 0) {
     if (cudaMemsetAsync(dH, 0, (size_t)p.n_rows * p.hidden * 4, st) != cudaSuccess) return FLCE_ERR_CUDA;
     if (cudaMemsetAsync(dW, 0, (size_t)p.vocab * p.hidden * 4, st) != cudaSuccess) return FLCE_ERR_CUDA;
@@ -1012,8 +1137,9 @@ static flce_status run_backward_any(const flce_problem& p, const Plan& pl, const
   choose_backward_chunk(plc, pc, sms);
   Maps mpc;
   if (!build_maps(pc, plc, Hc, W, dHc, dW, ws, true, &mpc)) return FLCE_ERR_CUDA;
-  flce_status r = sorted ? run_backward_sorted(pc, plc, pl, mpc, Hc, W, yc, lsec, dW, ws, sms, st, bias, rsc, dbias)
-                         : run_backward(pc, plc, mpc, yc, lsec, ws, sms, st, bias, rsc, dbias);
+  flce_status r = sorted ? run_backward_sorted(pc, plc, pl, mpc, Hc, W, yc, lsec, dW, ws, sms, st, bias, rsc, dbias,
+                                               opt)
+                         : run_backward(pc, plc, mpc, yc, lsec, ws, sms, st, bias, rsc, dbias, nullptr, nullptr, opt);
   if (r != FLCE_OK) return r;
   scatter_rows_kernel<<<(unsigned)p.n_rows, 256, 0, st>>>(reinterpret_cast<const float4*>(dHc), (int)(p.hidden / 4),
                                                           pos, reinterpret_cast<float4*>(dH));
@@ -1144,6 +1270,46 @@ flce_status flce_forward_backward(const flce_problem* p, const void* H, const vo
   return run_backward_any(*p, pl, mp, H, W, y, lse_buf, dH, dW, wsb, sms, st, nullptr, nullptr, nullptr);
 }
 
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+flce_status flce_forward_backward_adamw(const flce_problem* p, const void* H, const void* W, const int64_t* y,
+                                        float grad_loss, float* lse, float* loss, float* dH, float* w_master,
+                                        float* adam_m, float* adam_v, void* w_out, const flce_adamw_hparams* hp,
+                                        void* ws, size_t ws_bytes, void* stream) {
+  flce_status s = check_common(p, H, W, y, loss, ws, ws_bytes);
+  if (s != FLCE_OK) return s;
+  if (!dH || !w_master || !adam_m || !adam_v || !w_out || !hp) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(grad_loss)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(hp, 8)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(dH, 16) || !aligned(w_master, 16) || !aligned(adam_m, 16) || !aligned(adam_v, 16) ||
+      !aligned(w_out, 16))
+    return FLCE_ERR_UNSUPPORTED;
+  if (p->n_rows < 1 || p->n_rows > kRowChunk) return FLCE_ERR_UNSUPPORTED;
+  const size_t wbytes = (size_t)p->vocab * p->hidden * 2;
+  if (overlaps(w_out, wbytes, W, wbytes)) return FLCE_ERR_INVALID_ARGUMENT;
+  int sms = 0;
+  if (!device_setup(&sms)) return FLCE_ERR_CUDA;
+  Plan pl = make_plan(*p);
+  choose_backward_chunk(pl, *p, sms);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* lse_buf = lse ? lse : reinterpret_cast<float*>(wsb + pl.off_lse);
+  Maps mp;
+  if (!build_maps(*p, pl, H, W, dH, nullptr, wsb, true, &mp)) return FLCE_ERR_CUDA;
+  flce_status r = run_forward(*p, pl, mp, y, lse_buf, loss, grad_loss, wsb, sms, st);
+  if (r != FLCE_OK) return r;
+  {
+    ProfScope prof(FLCE_KERNEL_ADAMW_PREP, st);
+    adamw_prep_kernel<<<1, 32, 0, st>>>(hp, reinterpret_cast<WsHeader*>(wsb));
+    if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
+  }
+  const OptTarget opt{w_master, adam_m, adam_v, static_cast<__nv_bfloat16*>(w_out)};
+  return run_backward_any(*p, pl, mp, H, W, y, lse_buf, dH, nullptr, wsb, sms, st, nullptr, nullptr, nullptr, &opt);
+}
+
 flce_status flce_forward_ex(const flce_problem* p, int32_t reduction, const void* H, const void* W, const float* bias,
                             const int64_t* y, float* lse, float* loss, void* ws, size_t ws_bytes, void* stream) {
   flce_status s = check_common(p, H, W, y, loss, ws, ws_bytes, true);
@@ -1224,6 +1390,7 @@ flce_status flce_get_device_status(void* ws, void* stream) {
   const uint32_t zero = 0;
   if (cudaMemcpy(ws, &zero, sizeof(uint32_t), cudaMemcpyHostToDevice) != cudaSuccess) return FLCE_ERR_CUDA;
   if (status & kDevTimeout) return FLCE_ERR_TIMEOUT;
+  if (status & kDevBadHparams) return FLCE_ERR_INVALID_ARGUMENT;
   if (status & kDevBadTarget) return FLCE_ERR_BAD_TARGET;
   return FLCE_OK;
 }

@@ -20,7 +20,12 @@
 //     EPI_STORE  fp32 tile times a device scalar, stored by TMA;
 //     EPI_REDUCE fp32 tile times a device scalar, added into global memory
 //                by a TMA reduce-add (one writer per element per launch, so
-//                the summation order is fixed by the launch order).
+//                the summation order is fixed by the launch order);
+//     EPI_ADAMW  fp32 weight-gradient tile times a device scalar, consumed
+//                at once by an AdamW update of the weights it belongs to
+//                (fp32 master, moments, bf16 copy) and never stored.
+// STORE and REDUCE may also write through a row map (plain stores or
+// vector reductions instead of TMA) when the rows are in a sorted order.
 //
 // The accumulator of tile i lives in TMEM buffer i % 2, so the MMA of the next
 // tile overlaps the epilogue of the current one. Operands may be K-major or
@@ -51,11 +56,17 @@ constexpr uint32_t kGemmSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + k
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum EpiMode : int32_t { EPI_LSE = 0, EPI_DZ = 1, EPI_STORE = 2, EPI_REDUCE = 3 };
+enum EpiMode : int32_t { EPI_LSE = 0, EPI_DZ = 1, EPI_STORE = 2, EPI_REDUCE = 3, EPI_ADAMW = 4 };
+
+// Device constants of one fused AdamW step, in the order the epilogue reads
+// them: lr / (1 - beta1^t), 1 / sqrt(1 - beta2^t), 1 - lr * weight_decay,
+// beta1, beta2, eps.
+constexpr int kAdamwConsts = 6;
 
 // Device status bits (OR-ed into the workspace status word).
 constexpr uint32_t kDevBadTarget = 1u;
 constexpr uint32_t kDevTimeout = 2u;
+constexpr uint32_t kDevBadHparams = 4u;
 
 struct GemmParams {
   int32_t m_tiles, n_tiles, k_blocks;
@@ -74,7 +85,7 @@ struct GemmParams {
   int32_t part_ld;             // LSE: leading dimension of the partial arrays
   int32_t part_t0;             // LSE: partial index of n-tile 0
   int32_t filter;              // DZ: write the per-tile skip flags
-  int32_t skip_by_flags;       // STORE/REDUCE: leave out k-blocks whose dZ tiles were filtered
+  int32_t skip_by_flags;       // STORE/REDUCE/ADAMW: leave out k-blocks whose dZ tiles were filtered
   float filter_eps;
   int64_t ignore_index;
   const int64_t* y;
@@ -85,9 +96,10 @@ struct GemmParams {
   float* part_s;               // LSE: sum of 2^(t - max)       [tiles][part_ld]
   float* zy;                   // LSE: target logit per local row
   const float* scale;          // STORE / REDUCE: device scalar multiplier
-  uint32_t* flags;             // per staging tile: 4 quarter flags packed in one word
-  int32_t flags_ld;            // staging tiles per staging row-tile
-  int32_t flags_a_is_rows;     // REDUCE/STORE skip lookup: 1 = K indexes staging columns (dH)
+  uint32_t* flags;             // DZ: per staging tile, 4 quarter flags packed in one word
+  int32_t flags_ld;            // DZ: staging tiles per staging row-tile
+  int32_t flags_a_is_rows;     // skip lookup: 1 = K indexes staging columns (dH), 0 = staging rows (dW)
+  const uint64_t* keep;        // skip lookup: the chunk's keep masks (see tile_keep)
   // STORE / REDUCE with a row map: local row r is written to row
   // out_rows[out_m0 + r] of out_ptr (leading dimension out_ld, out_cols
   // columns) by plain stores or vector reductions instead of TMA; rows with
@@ -97,6 +109,13 @@ struct GemmParams {
   int64_t out_ld;
   int32_t out_cols;
   int32_t out_rows_n;
+  // EPI_ADAMW: the tile is the gradient of rows of the fp32 master weights
+  // out_ptr; it updates them, the moments opt_m / opt_v (same layout) and
+  // writes the bf16 copy opt_w, and the gradient itself is dropped.
+  const float* opt;            // kAdamwConsts device values
+  float* opt_m;
+  float* opt_v;
+  __nv_bfloat16* opt_w;
   uint32_t* status;
   uint64_t wait_limit_ns;
 };
@@ -139,38 +158,32 @@ __device__ __forceinline__ void tile_coords(const GemmParams& p, int t, int clus
   mt = mg * cluster + rank;
 }
 
-// Whether k-block kb of tile (mt, nt) reads only dZ tiles whose gradient was
-// filtered out. Staging tiles are 128 rows x 256 columns.
-//   dH (flags_a_is_rows = 1): A = staging rows mt*128.., columns kb*64..
-//   dW (flags_a_is_rows = 0): A = staging^T, rows kb*64.., columns mt*128..
-__device__ __forceinline__ bool kblock_skipped(const GemmParams& p, int mt, int kb) {
-  if (!p.skip_by_flags) return false;
-  if (mt >= p.m_tiles) return true;            // the empty half of a cluster's last group
-  int srow, scol;
-  if (p.flags_a_is_rows) {
-    srow = mt;
-    scol = (kb * kBK) / kBN;
-  } else {
-    srow = (kb * kBK) / kBM;
-    scol = (mt * kBM) / kBN;
+// Which k-blocks of a dW or dH tile read some kept gradient. Before the
+// contractions of a staging chunk run, one small kernel turns the chunk's
+// per-tile flags (staging tiles are 128 rows x 256 columns) into two bit
+// masks, so a tile reads one 64-bit word instead of a flag per k-block:
+//   dH (flags_a_is_rows = 1): keep[mt] has bit j set when staging tile
+//       (mt, j) holds gradient; k-block kb reads staging columns kb*64..,
+//       i.e. unit j = kb*64/256;
+//   dW (flags_a_is_rows = 0): keep[c] has bit r set when staging tile (r, c)
+//       holds gradient; the tile's vocabulary rows mt*128.. lie in staging
+//       column tile c = mt*128/256, and k-block kb reads staging rows
+//       kb*64.., i.e. unit r = kb*64/128.
+// Bit u of the returned word is set when unit u holds gradient for any of
+// the `group` vertically adjacent tiles from mt_first (an SM pair, or a
+// cluster, leaves a k-block out only when every one of its tiles does).
+__device__ __forceinline__ uint64_t tile_keep(const GemmParams& p, int mt_first, int group) {
+  uint64_t k = 0ull;
+  for (int r = 0; r < group; ++r) {
+    const int mt = mt_first + r;
+    if (mt < p.m_tiles) k |= __ldg(p.keep + (p.flags_a_is_rows ? mt : (mt * kBM) / kBN));
   }
-  return __ldg(p.flags + (size_t)srow * p.flags_ld + scol) == 0u;
+  return k;
 }
 
-// A k-block is left out by the whole cluster only when every CTA of it skips it.
-template <int kCluster>
-__device__ __forceinline__ bool kblock_skipped_group(const GemmParams& p, int mt_first, int kb) {
-  bool all = true;
-#pragma unroll
-  for (int r = 0; r < kCluster; ++r) all = all && kblock_skipped(p, mt_first + r, kb);
-  return all;
-}
-
-// Runtime form of kblock_skipped_group for the epilogue.
-__device__ __forceinline__ bool kblock_skipped_n(const GemmParams& p, int mt_first, int group, int kb) {
-  for (int r = 0; r < group; ++r)
-    if (!kblock_skipped(p, mt_first + r, kb)) return false;
-  return true;
+__device__ __forceinline__ bool kblock_dropped(const GemmParams& p, uint64_t keep, int kb) {
+  const int unit = p.flags_a_is_rows ? (kb * kBK) / kBN : (kb * kBK) / kBM;
+  return ((keep >> unit) & 1ull) == 0ull;
 }
 
 __device__ __forceinline__ void record_timeout(uint32_t* status, volatile uint32_t* abort_flag) {
@@ -194,8 +207,23 @@ struct AccRelease {
   }
 };
 
+// Epilogue sets a kernel instance is built with: the forward's launches
+// need only EPI_LSE, the backward's EPI_DZ, EPI_STORE and EPI_REDUCE, the
+// fused optimizer's also EPI_ADAMW. An instance carries only its set's code.
+constexpr int kModeLse = 1 << EPI_LSE;
+constexpr int kModeDz = 1 << EPI_DZ;
+constexpr int kModeStore = (1 << EPI_STORE) | (1 << EPI_REDUCE);
+constexpr int kModeAdamw = 1 << EPI_ADAMW;
+constexpr int kModesForward = kModeLse;
+constexpr int kModesBackward = kModeDz | kModeStore;
+constexpr int kModesBackwardAdamw = kModesBackward | kModeAdamw;
+constexpr int kModesAll = kModeLse | kModeDz | kModeStore | kModeAdamw;
+
 // `group` CTAs compute each tile group together (1, or 2 for the pair
 // kernel); a k-block left out of the MMAs is one every CTA of the group skips.
+// A problem whose mode is not in kModes (the host never launches one) only
+// releases the accumulator.
+template <int kModes = kModesAll>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtensorMap* tmOut, int mt, int nt,
                                               uint32_t taddr, int q, int lane, uint8_t* my_boxes, uint32_t& ebuf,
                                               const AccRelease& rel, int group = 1) {
@@ -206,7 +234,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) rel.arrive();
-  } else if (p.mode == EPI_LSE) {
+  } else if ((kModes & kModeLse) && p.mode == EPI_LSE) {
     const bool in_rows = lrow < p.m_valid && (p.row0 + lrow) < p.n_rows;
     const int grow = p.row0 + lrow;
     const int col_t0 = p.col0 + nt * kBN;
@@ -261,7 +289,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
       p.part_s[idx] = run_sum;
       if (has_t) p.zy[lrow] = zt;
     }
-  } else if (p.mode == EPI_DZ) {
+  } else if ((kModes & kModeDz) && p.mode == EPI_DZ) {
     const int grow = p.row0 + lrow;
     const bool in_rows = lrow < p.m_valid && grow < p.n_rows;
     const int col_t0 = p.col0 + nt * kBN;
@@ -347,15 +375,84 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
       const unsigned keep = __any_sync(0xffffffffu, amax >= p.filter_eps) ? 1u : 0u;
       if (lane == 0) reinterpret_cast<uint8_t*>(p.flags + (size_t)mt * p.flags_ld + nt)[q] = (uint8_t)keep;
     }
-  } else {
-    // EPI_STORE / EPI_REDUCE
-    bool all_skipped = p.skip_by_flags != 0;
-    if (p.skip_by_flags) {
-      const int mt_first = mt - mt % group;
-      for (int kb = 0; kb < p.k_blocks && all_skipped; ++kb) all_skipped = kblock_skipped_n(p, mt_first, group, kb);
-    }
+  } else if ((kModes & (kModeStore | kModeAdamw)) && ((1 << p.mode) & (kModeStore | kModeAdamw))) {
+    // EPI_STORE / EPI_REDUCE / EPI_ADAMW
+    const bool all_skipped = p.skip_by_flags != 0 && tile_keep(p, mt - mt % group, group) == 0ull;
     const float sc = __ldg(p.scale);
-    if (p.out_rows) {
+    if ((kModes & kModeAdamw) && p.mode == EPI_ADAMW) {
+      // AdamW on the finished gradient tile (the FORGE explainer's fused
+      // optimizer): one thread per weight row, 16 columns at a time; rows go
+      // through out_rows when the vocabulary runs in sorted order.
+      const float step_size = __ldg(p.opt + 0), rs2 = __ldg(p.opt + 1), decay = __ldg(p.opt + 2);
+      const float b1 = __ldg(p.opt + 3), b2 = __ldg(p.opt + 4), eps = __ldg(p.opt + 5);
+      const int srow = p.out_m0 + lrow;
+      const bool row_ok = lrow < p.m_valid && srow < p.out_rows_n;
+      const int64_t drow = row_ok ? (p.out_rows ? (int64_t)__ldg(p.out_rows + srow) : (int64_t)srow) : 0;
+      float* prow = p.out_ptr + drow * p.out_ld;
+      float* mrow = p.opt_m + drow * p.out_ld;
+      float* vrow = p.opt_v + drow * p.out_ld;
+      __nv_bfloat16* wrow = p.opt_w + drow * p.out_ld;
+#pragma unroll 1
+      for (int c = 0; c < kBN; c += 32) {
+        float x[32];
+        if (all_skipped) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = 0.f;
+        } else {
+          uint32_t r[32];
+          ptx::tmem_ld_32x32b_x32(taddr + c, r);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * sc;
+        }
+        if (!row_ok) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c0 = nt * kBN + c + 16 * h;   // out_cols is a multiple of 8
+          float4 pv[4], mv[4], vv[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (c0 + 4 * j < p.out_cols) {
+              pv[j] = *reinterpret_cast<const float4*>(prow + c0 + 4 * j);
+              mv[j] = *reinterpret_cast<const float4*>(mrow + c0 + 4 * j);
+              vv[j] = *reinterpret_cast<const float4*>(vrow + c0 + 4 * j);
+            }
+          }
+          uint32_t wb[8];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float* pe = &pv[j].x;
+            float* me = &mv[j].x;
+            float* ve = &vv[j].x;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float g = x[16 * h + 4 * j + e];
+              const float m = fmaf(b1, me[e], (1.f - b1) * g);
+              const float v = fmaf(b2, ve[e], (1.f - b2) * g * g);
+              me[e] = m;
+              ve[e] = v;
+              pe[e] = pe[e] * decay - step_size * (m / (sqrtf(v) * rs2 + eps));
+            }
+            __nv_bfloat162 lo = __floats2bfloat162_rn(pe[0], pe[1]), hi = __floats2bfloat162_rn(pe[2], pe[3]);
+            wb[2 * j] = *reinterpret_cast<uint32_t*>(&lo);
+            wb[2 * j + 1] = *reinterpret_cast<uint32_t*>(&hi);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (c0 + 4 * j < p.out_cols) {
+              *reinterpret_cast<float4*>(prow + c0 + 4 * j) = pv[j];
+              *reinterpret_cast<float4*>(mrow + c0 + 4 * j) = mv[j];
+              *reinterpret_cast<float4*>(vrow + c0 + 4 * j) = vv[j];
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            if (c0 + 8 * q < p.out_cols)
+              *reinterpret_cast<uint4*>(wrow + c0 + 8 * q) = make_uint4(wb[4 * q], wb[4 * q + 1], wb[4 * q + 2],
+                                                                        wb[4 * q + 3]);
+        }
+      }
+    } else if (p.out_rows) {
       // Row-mapped output (a vocabulary visited in sorted order writes dW
       // rows back in id order): one thread per row, 128 contiguous bytes
       // per 32-column slice. The map is a permutation of the output rows.
@@ -427,6 +524,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
         ebuf ^= 1u;
       }
     }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) rel.arrive();
+  } else {
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) rel.arrive();
@@ -507,9 +608,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
         tile_coords(p, tl, kCluster, rank, mt, nt);
         const int mt_first = mt - rank;
         const bool may_skip = p.skip_by_flags != 0;
+        const uint64_t keep = may_skip ? tile_keep(p, mt_first, kCluster) : ~0ull;
         const int k_blocks = p.k_blocks;
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (may_skip && kblock_skipped_group<kCluster>(p, mt_first, kb)) continue;
+          if (may_skip && kblock_dropped(p, keep, kb)) continue;
           if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
@@ -583,9 +685,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
         const uint32_t d_tmem = tmem_base + buf * kBN;
         uint32_t accumulate = 0;
         const bool may_skip = p.skip_by_flags != 0;
+        const uint64_t keep = may_skip ? tile_keep(p, mt_first, kCluster) : ~0ull;
+        const uint64_t own_keep = may_skip ? tile_keep(p, mt, 1) : ~0ull;
         const int k_blocks = p.k_blocks;
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (may_skip && kblock_skipped_group<kCluster>(p, mt_first, kb)) continue;
+          if (may_skip && kblock_dropped(p, keep, kb)) continue;
           if (!ptx::mbar_wait_bounded(&full_bar[stage], phase, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
@@ -595,7 +699,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
           // In a cluster, a stage the group loads for the peer may still be
           // one this CTA's own tile skips: it then issues no MMA but still
           // releases the stage.
-          if (kCluster == 1 || !may_skip || !kblock_skipped(p, mt, kb)) {
+          if (kCluster == 1 || !may_skip || !kblock_dropped(p, own_keep, kb)) {
             const uint32_t a_addr = smem_base + stage * kStageBytes;
             const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll

@@ -22,27 +22,40 @@
 namespace flce {
 
 constexpr int kPairStages = 6;
+constexpr int kPairStagesLse = 7;     // launches of EPI_LSE problems only: no store boxes
 constexpr uint32_t kPairBBytes = (kBN / 2) * kBK * 2;           // 16 KiB: this CTA's half of B
 constexpr uint32_t kPairStageBytes = kABytes + kPairBBytes;      // 32 KiB
-constexpr uint32_t kPairSmemBytes = 1024 + kPairStages * kPairStageBytes + kEpiBytes + kBarrierBytes;
-static_assert(kPairSmemBytes <= 232448, "shared memory of the pair kernel");
+
+// The epilogue's TMA store boxes take the room of one more stage; EPI_LSE
+// stores nothing through shared memory, so the forward's instance uses that
+// room for a seventh stage.
+__host__ __device__ constexpr int pair_stages(int modes) { return modes == kModesForward ? kPairStagesLse : kPairStages; }
+__host__ __device__ constexpr uint32_t pair_epi_bytes(int modes) { return modes == kModesForward ? 0u : kEpiBytes; }
+__host__ __device__ constexpr uint32_t pair_smem_bytes(int modes) {
+  return 1024 + pair_stages(modes) * kPairStageBytes + pair_epi_bytes(modes) + kBarrierBytes;
+}
+static_assert(pair_smem_bytes(kModesBackward) <= 232448 && pair_smem_bytes(kModesForward) <= 232448,
+              "shared memory of the pair kernel");
+static_assert((2 * kPairStagesLse + 5) * 8 + 8 <= kBarrierBytes, "barrier area of the pair kernel");
 
 // kSkip: some problem of the launch leaves out filtered k-blocks. Launches
 // without filtering use the kSkip = false instance, whose k-loops carry no
-// skip test at all.
-template <bool kSkip>
+// skip test at all. kModes: the epilogue set (kModesForward,
+// kModesBackward or kModesBackwardAdamw), which also fixes the ring depth.
+template <bool kSkip, int kModes>
 __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const __grid_constant__ GemmLaunch L) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-  uint8_t* epi_smem = smem + kPairStages * kPairStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + kEpiBytes);
-  uint64_t* full_bar = bars;                        // [kPairStages] (used in the even CTA)
-  uint64_t* empty_bar = bars + kPairStages;         // [kPairStages]
-  uint64_t* acc_full = bars + 2 * kPairStages;      // [2]
-  uint64_t* acc_empty = bars + 2 * kPairStages + 2; // [2] (used in the even CTA)
-  uint64_t* drain_bar = bars + 2 * kPairStages + 4;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kPairStages + 5);
+  constexpr int kStg = pair_stages(kModes);
+  uint8_t* epi_smem = smem + kStg * kPairStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi_smem + pair_epi_bytes(kModes));
+  uint64_t* full_bar = bars;                        // [kStg] (used in the even CTA)
+  uint64_t* empty_bar = bars + kStg;         // [kStg]
+  uint64_t* acc_full = bars + 2 * kStg;      // [2]
+  uint64_t* acc_empty = bars + 2 * kStg + 2; // [2] (used in the even CTA)
+  uint64_t* drain_bar = bars + 2 * kStg + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStg + 5);
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -57,7 +70,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
   constexpr uint16_t kBoth = 3;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPairStages; ++s) {
+    for (int s = 0; s < kStg; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
       ptx::mbar_init(&empty_bar[s], 1);
     }
@@ -89,8 +102,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
     if (lane == 0) {
       const uint32_t full_leader = ptx::map_to_rank(&full_bar[0], 0);
       uint32_t stage = 0, phase = 0;
-      int32_t last_parity[kPairStages];
-      for (int s = 0; s < kPairStages; ++s) last_parity[s] = -1;
+      int32_t last_parity[kStg];
+      for (int s = 0; s < kStg; ++s) last_parity[s] = -1;
       bool ok = true;
       for (int t = unit0; t < num_tiles && ok; t += unit_stride) {
         int pi, mt, nt;
@@ -100,9 +113,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
         const CUtensorMap* tmB = &L.tm_b[pi];
         tile_coords(p, tl, 2, rank, mt, nt);
         const bool may_skip = kSkip && p.skip_by_flags != 0;
+        const uint64_t keep = may_skip ? tile_keep(p, mt - rank, 2) : ~0ull;
         const int k_blocks = p.k_blocks;
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (kSkip && may_skip && kblock_skipped_group<2>(p, mt - rank, kb)) continue;
+          if (kSkip && may_skip && kblock_dropped(p, keep, kb)) continue;
           if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
@@ -127,7 +141,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
             ptx::tma_load_2d_pair(sb, tmB, p.b_k0 + kc, n_half, fb);
           }
           last_parity[stage] = (int32_t)phase;
-          if (++stage == kPairStages) {
+          if (++stage == kStg) {
             stage = 0;
             phase ^= 1u;
           }
@@ -137,7 +151,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
         // The even CTA's full barriers count both CTAs' bytes: once a phase
         // completes, no copy of that phase is still landing in either CTA.
         volatile uint32_t never = 0u;
-        for (int s = 0; s < kPairStages; ++s)
+        for (int s = 0; s < kStg; ++s)
           if (last_parity[s] >= 0) ptx::mbar_wait_bounded(&full_bar[s], (uint32_t)last_parity[s], 100000000ull, &never);
       }
     }
@@ -166,9 +180,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
         uint32_t accumulate = 0;
         const bool a_mn = p.a_mn != 0, b_mn = p.b_mn != 0;
         const bool may_skip = kSkip && p.skip_by_flags != 0;
+        const uint64_t keep = may_skip ? tile_keep(p, mt, 2) : ~0ull;   // mt: the even CTA's m-tile
         const int k_blocks = p.k_blocks;
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (kSkip && may_skip && kblock_skipped_group<2>(p, mt, kb)) continue;   // mt: the even CTA's m-tile
+          if (kSkip && may_skip && kblock_dropped(p, keep, kb)) continue;
           if (!ptx::mbar_wait_bounded(&full_bar[stage], phase, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
@@ -187,7 +202,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
             accumulate = 1;
           }
           ptx::mma_commit_pair_multicast(&empty_bar[stage], kBoth);
-          if (++stage == kPairStages) {
+          if (++stage == kStg) {
             stage = 0;
             phase ^= 1u;
           }
@@ -221,7 +236,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
       ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + buf * kBN + ((uint32_t)(q * 32) << 16);
       const AccRelease rel{&acc_empty[buf], ptx::map_to_rank(&acc_empty[buf], 0), !leader};
-      epilogue_tile(p, tmOut, mt, nt, taddr, q, lane, my_boxes, ebuf, rel, 2);
+      epilogue_tile<kModes>(p, tmOut, mt, nt, taddr, q, lane, my_boxes, ebuf, rel, 2);
     }
     if (lane == 0) ptx::bulk_wait_group<0>();
     __syncwarp();

@@ -13,7 +13,7 @@
 //   hmean_kernel          fixed-order sum of the splits / count
 //   avg_logit_kernel      a_v in fp32, and a 32-bit key whose ascending order
 //                         is the descending order of a_v
-//   radix_sort_kernel     stable LSD radix sort of the keys (one block)
+//   radix_*_kernel        stable LSD radix sort of the keys
 //   gather_vocab_kernel   W and the bias rearranged in the sorted order
 //   remap_targets_kernel  each target replaced by its sorted position
 #pragma once
@@ -26,9 +26,6 @@ namespace flce {
 constexpr int kHsumMaxSplits = 256;    // row splits of the column sums
 constexpr int kHsumRowsPerSplit = 32;  // fewest rows a split gets before splits are added
 constexpr int kHsumCols = 2048;        // columns per block: 8 per thread
-constexpr int kSortThreads = 1024;
-constexpr int kSortWarps = kSortThreads / 32;
-constexpr int kSortBatch = 8;          // keys a lane loads ahead in the scatter
 constexpr int kVocabWarpsPerBlock = 8;
 
 __device__ __forceinline__ bool sort_target_valid(int64_t t, int64_t vocab, int64_t ignore_index) {
@@ -132,96 +129,126 @@ __global__ void __launch_bounds__(kVocabWarpsPerBlock * 32) avg_logit_kernel(
   }
 }
 
-// Stable LSD radix sort of n 32-bit keys, 8-bit digits, four passes, in one
-// block of 32 warps. Warp w owns the contiguous segment w of the array. Each
-// pass counts every warp's digits, turns the counts into an output offset per
-// (digit, warp) in digit-major, warp-minor order, and scatters each warp's
-// segment in its original order (ranks among equal digits from
-// __match_any_sync), so equal digits keep their relative order and the
-// output positions form a permutation of [0, n). ids start as 0..n-1. On
-// return keys_a/ids_a hold the sorted keys and ids and inv[ids_a[i]] = i.
-__global__ void __launch_bounds__(kSortThreads, 1) radix_sort_kernel(uint32_t* __restrict__ keys_a,
-                                                                    uint32_t* __restrict__ keys_b,
-                                                                    int32_t* __restrict__ ids_a,
-                                                                    int32_t* __restrict__ ids_b,
-                                                                    int32_t* __restrict__ inv, int n) {
-  __shared__ uint32_t offs[kSortWarps][256];
-  __shared__ uint32_t digit_base[256];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int seg = (int)(((int64_t)n + kSortWarps - 1) / kSortWarps);
-  const int s0 = min(n, warp * seg), s1 = min(n, s0 + seg);
-  uint32_t* kin = keys_a;
-  uint32_t* kout = keys_b;
-  int32_t* iin = ids_a;
-  int32_t* iout = ids_b;
-#pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = pass * 8;
-    for (int i = threadIdx.x; i < kSortWarps * 256; i += kSortThreads) (&offs[0][0])[i] = 0u;
-    __syncthreads();
-#pragma unroll 4
-    for (int i = s0 + lane; i < s1; i += 32) atomicAdd(&offs[warp][(kin[i] >> shift) & 255u], 1u);
-    __syncthreads();
-    if (threadIdx.x < 256) {
-      const int dg = threadIdx.x;
-      uint32_t run = 0;
-      for (int w = 0; w < kSortWarps; ++w) {
-        const uint32_t c = offs[w][dg];
-        offs[w][dg] = run;
-        run += c;
-      }
-      digit_base[dg] = run;
+// Stable LSD radix sort of n 32-bit keys with their ids: 8-bit digits, four
+// passes, each of three launches over tiles of kSortTile keys (one block per
+// tile). For pass `shift`:
+//   radix_hist_kernel     digit counts of every tile, hist[d * tiles + b];
+//   radix_scan_kernel     exclusive prefix sums of hist in that (digit-major,
+//                         tile-minor) order: where tile b's keys of digit d go;
+//   radix_scatter_kernel  each key to that offset plus its rank among the
+//                         tile's keys of the same digit, counted in tile order.
+// Ranks keep the input order of equal digits, so every pass is stable and the
+// output positions are a permutation of [0, n). radix_inverse_kernel then
+// writes inv[ids[i]] = i.
+constexpr int kSortTile = 4096;
+constexpr int kSortWarpsPerTile = 8;                      // 256 threads
+constexpr int kSortWarpKeys = kSortTile / kSortWarpsPerTile;
+
+__global__ void __launch_bounds__(256) radix_hist_kernel(const uint32_t* __restrict__ keys, int n, int shift,
+                                                         uint32_t* __restrict__ hist) {
+  __shared__ uint32_t cnt[256];
+  const int b = blockIdx.x, lane = threadIdx.x & 31;
+  cnt[threadIdx.x] = 0u;
+  __syncthreads();
+  const int t0 = b * kSortTile, t1 = min(n, t0 + kSortTile);
+  for (int base = t0; base < t1; base += 256) {
+    const int i = base + threadIdx.x;
+    const bool act = i < t1;
+    const unsigned mask = __ballot_sync(0xffffffffu, act);
+    if (act) {
+      const uint32_t d = (keys[i] >> shift) & 255u;
+      const unsigned peers = __match_any_sync(mask, d);
+      if ((peers & ((1u << lane) - 1u)) == 0u) atomicAdd(&cnt[d], (uint32_t)__popc(peers));
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t run = 0;
-      for (int dg = 0; dg < 256; ++dg) {
-        const uint32_t c = digit_base[dg];
-        digit_base[dg] = run;
-        run += c;
-      }
-    }
-    __syncthreads();
-    if (threadIdx.x < 256)
-      for (int w = 0; w < kSortWarps; ++w) offs[w][threadIdx.x] += digit_base[threadIdx.x];
-    __syncthreads();
-#pragma unroll 1
-    for (int base = s0; base < s1; base += 32 * kSortBatch) {
-      uint32_t kk[kSortBatch];
-      int32_t ii[kSortBatch];
-#pragma unroll
-      for (int b = 0; b < kSortBatch; ++b) {
-        const int i = base + b * 32 + lane;
-        kk[b] = i < s1 ? kin[i] : 0u;
-        ii[b] = i < s1 ? (pass == 0 ? i : iin[i]) : 0;
-      }
-#pragma unroll
-      for (int b = 0; b < kSortBatch; ++b) {
-        const int i = base + b * 32 + lane;
-        const bool act = i < s1;
-        const unsigned mask = __ballot_sync(0xffffffffu, act);
-        if (act) {
-          const uint32_t dg = (kk[b] >> shift) & 255u;
-          const unsigned peers = __match_any_sync(mask, dg);
-          const int rank = __popc(peers & ((1u << lane) - 1u));
-          const uint32_t pos = offs[warp][dg] + (uint32_t)rank;
-          kout[pos] = kk[b];
-          iout[pos] = ii[b];
-          __syncwarp(mask);
-          if (rank == 0) offs[warp][dg] += (uint32_t)__popc(peers);
-        }
-        __syncwarp();
-      }
-    }
-    __syncthreads();
-    uint32_t* tk = kin;
-    kin = kout;
-    kout = tk;
-    int32_t* ti = iin;
-    iin = iout;
-    iout = ti;
   }
-  for (int i = threadIdx.x; i < n; i += kSortThreads) inv[iin[i]] = i;
+  __syncthreads();
+  hist[(size_t)threadIdx.x * gridDim.x + b] = cnt[threadIdx.x];
+}
+
+__global__ void __launch_bounds__(1024) radix_scan_kernel(uint32_t* __restrict__ hist, int count) {
+  __shared__ uint32_t part[1024];
+  const int per = (count + 1023) / 1024;
+  const int s0 = min(count, (int)threadIdx.x * per), s1 = min(count, s0 + per);
+  uint32_t sum = 0u;
+  for (int i = s0; i < s1; ++i) sum += hist[i];
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {
+    const uint32_t v = threadIdx.x >= (unsigned)o ? part[threadIdx.x - o] : 0u;
+    __syncthreads();
+    part[threadIdx.x] += v;
+    __syncthreads();
+  }
+  uint32_t run = threadIdx.x ? part[threadIdx.x - 1] : 0u;
+  for (int i = s0; i < s1; ++i) {
+    const uint32_t c = hist[i];
+    hist[i] = run;
+    run += c;
+  }
+}
+
+// Warp w of the block takes keys [w * 512, (w + 1) * 512) of the tile in
+// chunks of 32: first it counts its digits, then each key's output position
+// is the tile's offset for the digit, plus the counts of earlier warps, plus
+// the warp's running count, plus the key's rank among lower lanes of its
+// chunk with the same digit. ids_in == nullptr means ids 0..n-1.
+__global__ void __launch_bounds__(256) radix_scatter_kernel(const uint32_t* __restrict__ keys_in,
+                                                            const int32_t* __restrict__ ids_in, int n, int shift,
+                                                            const uint32_t* __restrict__ offs,
+                                                            uint32_t* __restrict__ keys_out,
+                                                            int32_t* __restrict__ ids_out) {
+  __shared__ uint32_t wpos[kSortWarpsPerTile][256];
+  const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = b * kSortTile, t1 = min(n, t0 + kSortTile);
+  const int w0 = min(t1, t0 + warp * kSortWarpKeys), w1 = min(t1, w0 + kSortWarpKeys);
+  const unsigned below = (1u << lane) - 1u;
+  for (int i = threadIdx.x; i < kSortWarpsPerTile * 256; i += 256) (&wpos[0][0])[i] = 0u;
+  __syncthreads();
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const bool act = i < w1;
+    const unsigned mask = __ballot_sync(0xffffffffu, act);
+    if (act) {
+      const uint32_t d = (keys_in[i] >> shift) & 255u;
+      const unsigned peers = __match_any_sync(mask, d);
+      if ((peers & below) == 0u) wpos[warp][d] += (uint32_t)__popc(peers);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  {
+    const int d = threadIdx.x;
+    uint32_t run = offs[(size_t)d * gridDim.x + b];
+    for (int w = 0; w < kSortWarpsPerTile; ++w) {
+      const uint32_t c = wpos[w][d];
+      wpos[w][d] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int base = w0; base < w1; base += 32) {
+    const int i = base + lane;
+    const bool act = i < w1;
+    const unsigned mask = __ballot_sync(0xffffffffu, act);
+    if (act) {
+      const uint32_t k = keys_in[i];
+      const int32_t id = ids_in ? ids_in[i] : i;
+      const uint32_t d = (k >> shift) & 255u;
+      const unsigned peers = __match_any_sync(mask, d);
+      const uint32_t rank = (uint32_t)__popc(peers & below);
+      const uint32_t pos = wpos[warp][d] + rank;
+      keys_out[pos] = k;
+      ids_out[pos] = id;
+      __syncwarp(mask);
+      if (rank == 0u) wpos[warp][d] += (uint32_t)__popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void radix_inverse_kernel(const int32_t* __restrict__ ids, int n, int32_t* __restrict__ inv) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) inv[ids[i]] = i;
 }
 
 // Ws[i] = W[order[i]] (rows of row_vec 16-byte groups) and, with a bias,

@@ -21,7 +21,7 @@ def test_library_exports_every_declared_symbol():
                              "flce_get_device_status", "flce_status_string", "flce_get_filter_stats",
                              "flce_profile_set", "flce_profile_count", "flce_forward_static_scratch",
                              "flce_forward_ex", "flce_backward_ex", "flce_forward_workspace_bytes",
-                             "flce_get_vocab_order"}
+                             "flce_get_vocab_order", "flce_forward_backward_adamw"}
     out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
     for name in declared:
@@ -73,7 +73,7 @@ def test_sorted_vocabulary_workspace_and_getter_checks():
     srt = flce.make_problem(8192, 2048, 151552, flags=flce.FLAG_SORT_VOCAB)
     grow = flce.flce_workspace_bytes(srt) - flce.flce_workspace_bytes(base)
     v, d, n = 151552, 2048, 8192
-    assert v * d * 2 <= grow <= v * d * 2 + 28 * v + 8 * n + 1028 * d + 12 * 1024
+    assert v * d * 2 <= grow <= v * d * 2 + 29 * v + 8 * n + 1028 * d + 12 * 1024
     # The forward needs none of it.
     assert flce.flce_forward_workspace_bytes(srt) == flce.flce_forward_workspace_bytes(base)
     # Sorting and compaction together: the compaction buffers come after.
@@ -87,6 +87,32 @@ def test_sorted_vocabulary_workspace_and_getter_checks():
     assert st(srt, FAKE + 16, FAKE, None, 0) == Status.ERR_INVALID_ARGUMENT
     assert st(srt, FAKE, FAKE + 2, None, 0) == Status.ERR_INVALID_ARGUMENT
     assert st(None, FAKE, FAKE, None, 0) == Status.ERR_INVALID_ARGUMENT
+
+
+def test_fused_adamw_argument_checks():
+    assert ctypes.sizeof(flce.AdamwHparams) == 24
+    assert flce.AdamwHparams.step.offset == 20
+    good = flce.make_problem(16, 64, 100)
+    nb = flce.flce_workspace_bytes(good)
+    wbytes = 100 * 64 * 2
+    W_ = FAKE
+    out = FAKE + (1 << 24)
+
+    def call(prob=good, w_out=out, hp=FAKE, dH=FAKE, master=FAKE, n=nb):
+        return flce.flce_forward_backward_adamw(prob, FAKE, W_, FAKE, 1.0, None, FAKE, dH, master, FAKE, FAKE,
+                                                w_out, hp, FAKE, ws_bytes=n, stream=0)
+    assert call(hp=None) == Status.ERR_INVALID_ARGUMENT
+    assert call(hp=FAKE + 4) == Status.ERR_INVALID_ARGUMENT
+    assert call(master=None) == Status.ERR_INVALID_ARGUMENT
+    assert call(dH=None) == Status.ERR_INVALID_ARGUMENT
+    assert call(w_out=None) == Status.ERR_INVALID_ARGUMENT
+    assert call(w_out=W_ + wbytes - 16) == Status.ERR_INVALID_ARGUMENT     # overlaps W
+    assert call(master=FAKE + 8) == Status.ERR_UNSUPPORTED                 # not 16-byte aligned
+    assert call(n=nb - 1) == Status.ERR_WORKSPACE_TOO_SMALL
+    many = flce.make_problem(8193, 64, 100)
+    assert call(prob=many, n=flce.flce_workspace_bytes(many)) == Status.ERR_UNSUPPORTED
+    none = flce.make_problem(0, 64, 100)
+    assert call(prob=none, n=flce.flce_workspace_bytes(none)) == Status.ERR_UNSUPPORTED
 
 
 def test_workspace_bytes_rejects_bad_problems():

@@ -1,0 +1,149 @@
+"""GPU parity of flce_forward_backward_adamw (W's AdamW step fused into the dW
+contraction, as the FORGE explainer describes) against the fp64 oracle's
+two-phase step: gradient, then AdamW on the fp32 master weights."""
+
+import numpy as np
+import pytest
+import torch
+
+import lm_head_loss_gb300 as flce
+import oracle
+import synth
+from gpu_common import GRAD_REL, LOSS_REL, LSE_ABS, small_inputs, to_device
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+HP = {"lr": 2e-3, "beta1": 0.9, "beta2": 0.95, "eps": 1e-8, "weight_decay": 0.1}
+
+
+def _state(inp, seed):
+    """fp32 master weights near the bf16 W, and moments of a run in progress."""
+    rng = np.random.default_rng(seed)
+    w = synth.bf16_bits_to_f32(inp["W"])
+    master = (w + rng.standard_normal(w.shape).astype(np.float32) * np.float32(1e-3) * np.abs(w)).astype(np.float32)
+    m = (rng.standard_normal(w.shape) * 1e-4).astype(np.float32)
+    v = (rng.random(w.shape) * 1e-7 + 1e-8).astype(np.float32)
+    return master, m, v
+
+
+def _gpu_step(inp, master, m, v, step, flags=0):
+    H, W, y = to_device(inp)
+    dev = H.device
+    tm, tmm, tv = (torch.from_numpy(a.copy()).to(dev) for a in (master, m, v))
+    w_out = torch.empty(W.shape, dtype=torch.bfloat16, device=dev)
+    hp = flce.adamw_hparams(HP["lr"], step, (HP["beta1"], HP["beta2"]), HP["eps"], HP["weight_decay"], dev)
+    ws = flce.Workspace(dev)
+    loss, lse, dH = flce.forward_backward_adamw(H, W, y, tm, tmm, tv, w_out, hp, flags=flags, workspace=ws)
+    return {"loss": loss.item(), "lse": lse.cpu().numpy(), "dH": dH.cpu().numpy(), "master": tm.cpu().numpy(),
+            "m": tmm.cpu().numpy(), "v": tv.cpu().numpy(),
+            "w_out": w_out.view(torch.int16).cpu().numpy().view(np.uint16), "status": flce.device_status(ws)}
+
+
+def _tolerances(H64, W64, y, ref, step):
+    """Per-element bounds on the kernel's m, v and master after one step.
+
+    G is rounded to bf16 (relative 2^-9) before the fp32 contraction, so the
+    kernel's dW_vd is within 2^-7 * sum_n |dZ_nv| |H_nd| of the exact one;
+    that bound is carried through one AdamW step to first order."""
+    dZ = oracle.dlogits(H64, W64, y)
+    dg = 2.0 ** -7 * (np.abs(dZ).T @ np.abs(H64))
+    b1, b2, lr, eps = HP["beta1"], HP["beta2"], HP["lr"], HP["eps"]
+    bc1, bc2 = 1 - b1 ** step, 1 - b2 ** step
+    tol_m = (1 - b1) * dg + 1e-6 * np.abs(ref["m"]) + 1e-12
+    tol_v = (1 - b2) * (2 * np.abs(ref["dW"]) + dg) * dg + 1e-5 * ref["v"] + 1e-20
+    denom = np.sqrt(ref["v"] / bc2) + eps
+    d_denom = tol_v / (2 * np.sqrt(bc2) * np.sqrt(np.maximum(ref["v"], 1e-30)))
+    tol_p = lr / bc1 * (tol_m / denom + np.abs(ref["m"]) * d_denom / denom ** 2) * 1.5 + \
+        4 * 2.0 ** -24 * np.abs(ref["master"]) + 1e-12
+    return tol_m, tol_v, tol_p
+
+
+def _check(got, inp, master, m, v, step):
+    H64, W64 = oracle.inputs_f64(inp["H"], inp["W"])
+    ref = oracle.forward_backward_adamw(H64, W64, inp["y"], master.astype(np.float64), m.astype(np.float64),
+                                        v.astype(np.float64), {**HP, "step": step})
+    assert got["status"] == flce.Status.OK
+    assert abs(got["loss"] - ref["loss"]) <= LOSS_REL * max(abs(ref["loss"]), 1e-6)
+    assert np.max(np.abs(got["lse"] - ref["lse"])) <= LSE_ABS
+    s = float(np.max(np.abs(ref["dH"])))
+    assert float(np.max(np.abs(got["dH"] - ref["dH"]))) <= GRAD_REL * s if s > 0 else np.all(got["dH"] == 0)
+    tol_m, tol_v, tol_p = _tolerances(H64, W64, inp["y"], ref, step)
+    assert np.all(np.abs(got["m"] - ref["m"]) <= tol_m)
+    assert np.all(np.abs(got["v"] - ref["v"]) <= tol_v)
+    err_p = np.abs(got["master"] - ref["master"])
+    assert np.all(err_p <= tol_p), float(np.max(err_p / tol_p))
+    # The bf16 copy is the round-to-nearest-even of the kernel's own fp32 result.
+    assert np.array_equal(got["w_out"], synth.f64_to_bf16_bits(got["master"].astype(np.float64)))
+    # The step moved the weights by about lr, far more than the tolerance.
+    assert float(np.median(np.abs(ref["master"] - master))) > 20 * float(np.median(tol_p))
+    return ref
+
+
+@pytest.mark.parametrize("n,d,v,step", [(1000, 128, 5000, 3), (300, 72, 1000, 1), (4000, 64, 8192 + 100, 7)])
+def test_fused_adamw_matches_two_phase_oracle(n, d, v, step):
+    inp = small_inputs(n, d, v, seed=90 + n, targets="zipf", ignore=0.1)
+    master, m, vv = _state(inp, n)
+    got = _gpu_step(inp, master, m, vv, step)
+    _check(got, inp, master, m, vv, step)
+
+
+@pytest.mark.parametrize("flags", [flce.FLAG_SORT_VOCAB, flce.FLAG_COMPACT_IGNORED,
+                                   flce.FLAG_SORT_VOCAB | flce.FLAG_COMPACT_IGNORED])
+def test_fused_adamw_with_sorting_and_compaction(flags):
+    inp = small_inputs(2000, 128, 6000, seed=95, targets="zipf", ignore=0.4)
+    master, m, v = _state(inp, 5)
+    got = _gpu_step(inp, master, m, v, 4, flags)
+    _check(got, inp, master, m, v, 4)
+
+
+def test_fused_adamw_with_every_row_ignored_takes_a_zero_gradient_step():
+    inp = small_inputs(500, 64, 3000, seed=96, targets="zipf", ignore=1.0)
+    master, m, v = _state(inp, 6)
+    for flags in (0, flce.FLAG_COMPACT_IGNORED):
+        got = _gpu_step(inp, master, m, v, 2, flags)
+        assert got["loss"] == 0.0 and np.all(got["dH"] == 0.0)
+        _, m_ref, v_ref = oracle.adamw_step(master, np.zeros_like(master), m, v, 2, **HP)
+        assert np.max(np.abs(got["m"] - m_ref)) <= 1e-6 * np.max(np.abs(m_ref))
+        assert np.max(np.abs(got["v"] - v_ref)) <= 1e-6 * np.max(v_ref)
+
+
+def test_fused_adamw_rejects_bad_hyperparameters_on_the_device():
+    inp = small_inputs(200, 64, 1000, seed=97)
+    master, m, v = _state(inp, 7)
+    got = _gpu_step(inp, master, m, v, 0)              # step 0 has no bias correction
+    assert got["status"] == flce.Status.ERR_INVALID_ARGUMENT
+    assert np.array_equal(got["master"], master) and np.array_equal(got["m"], m) and np.array_equal(got["v"], v)
+
+
+def test_fused_adamw_head_three_steps():
+    # The wrapper keeps the state and alternates the two bf16 copies. It is
+    # started from a run in progress (moments set, ten steps taken) so that
+    # every step is well conditioned and the per-step bounds add up.
+    n, d, v = 1500, 128, 4000
+    inp = small_inputs(n, d, v, seed=98, targets="zipf", ignore=0.05)
+    H, W, y = to_device(inp)
+    head = flce.FusedAdamWHead(W, lr=HP["lr"], betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"],
+                               weight_decay=HP["weight_decay"])
+    _, m0, v0 = _state(inp, 8)
+    head.m.copy_(torch.from_numpy(m0))
+    head.v.copy_(torch.from_numpy(v0))
+    head.steps = 10
+    H64 = oracle.inputs_f64(inp["H"], inp["W"])[0]
+    p = synth.bf16_bits_to_f64(inp["W"])
+    p0 = p.copy()
+    mo, vo = m0.astype(np.float64), v0.astype(np.float64)
+    tol = np.zeros_like(p)
+    for t in range(11, 14):
+        w_cur = head.weight
+        loss, lse, dH = head.step(H, y)
+        assert head.weight.data_ptr() != w_cur.data_ptr()
+        w_bf16 = synth.bf16_bits_to_f64(synth.f64_to_bf16_bits(p))
+        r = oracle.forward_backward_adamw(H64, w_bf16, inp["y"], p, mo, vo, {**HP, "step": t})
+        assert abs(loss.item() - r["loss"]) <= LOSS_REL * abs(r["loss"])
+        tol += _tolerances(H64, w_bf16, inp["y"], r, t)[2]
+        p, mo, vo = r["master"], r["m"], r["v"]
+    got = head.master.cpu().numpy()
+    assert np.all(np.abs(got - p) <= 2 * tol), float(np.max(np.abs(got - p) / tol))
+    assert float(np.median(np.abs(p - p0))) > 20 * float(np.median(tol))
+    assert flce.device_status(head.workspace) == flce.Status.OK
