@@ -34,6 +34,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cstddef>
 #include <cstdint>
 
 #include "ptx_sm103.cuh"
@@ -68,7 +69,11 @@ constexpr uint32_t kDevBadTarget = 1u;
 constexpr uint32_t kDevTimeout = 2u;
 constexpr uint32_t kDevBadHparams = 4u;
 
-struct GemmParams {
+// Each problem's parameters start on a 128-byte boundary of the launch's
+// parameter block. Measured on GB300 with the same sources otherwise: with
+// sizes of 224, 264 or 320 bytes (or 64-byte alignment) the forward launch ran
+// about 11% slower, at higher SM clocks, than with 128-byte alignment.
+struct alignas(128) GemmParams {
   int32_t m_tiles, n_tiles, k_blocks;
   int32_t a_mn, b_mn;          // 1 if the operand is MN-major in global memory
   int32_t n_fast;              // tile raster: 1 = n index varies fastest
@@ -134,6 +139,9 @@ struct GemmLaunch {
   int32_t n_probs;
   int32_t tile_end[kMaxProblems];
 };
+static_assert(sizeof(GemmParams) % 128 == 0 && offsetof(GemmLaunch, prob) % 128 == 0,
+              "problem parameters on 128-byte boundaries");
+static_assert(sizeof(GemmLaunch) <= 4096, "kernel parameter block");
 
 // Tiles are counted in groups of kCluster vertically adjacent m-tiles that
 // share one n-tile (one group per cluster); with kCluster = 1 a group is a tile.
