@@ -54,7 +54,7 @@ def parse_args():
     ap.add_argument("--adamw", choices=["none", "fused", "two-phase"], default="none",
                     help="also take an AdamW step on W each step: fused into the dW contraction "
                          "(flce_forward_backward_adamw) or after it (flce_forward_backward, then "
-                         "torch.optim.AdamW(fused=True) on dW and a bf16 copy)")
+                         "flce_adamw_step on dW)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -269,18 +269,16 @@ def run_ours(args, rank, world, local):
                     raise flce.FlceError(st, "flce_forward_backward_adamw")
                 cur[0] = 1 - i
         else:
-            master.requires_grad_(True)
-            opt = torch.optim.AdamW([master], lr=1e-4, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1, fused=True)
+            hp = flce.adamw_hparams(1e-4, 10, (0.9, 0.95), 1e-8, 0.1, dev)
 
             def step():
                 i = cur[0]
                 st = flce.flce_forward_backward(prob, H, w_pair[i], y, 1.0, lse, loss, dH, dW, ws, stream=stream)
                 if st != flce.Status.OK:
                     raise flce.FlceError(st, "flce_forward_backward")
-                master.grad = dW
-                opt.step()
-                with torch.no_grad():
-                    w_pair[1 - i].copy_(master)
+                st = flce.flce_adamw_step(hp, dW, master, adam_m, adam_v, w_pair[1 - i], dW.numel(), ws, stream)
+                if st != flce.Status.OK:
+                    raise flce.FlceError(st, "flce_adamw_step")
                 cur[0] = 1 - i
 
     def barrier():
@@ -304,6 +302,7 @@ def run_ours(args, rank, world, local):
         step()
     torch.cuda.synchronize()
     launches_per_step = prof.count
+    one_step = [(k, round(ms, 4)) for k, ms in prof.launches()]
 
     cap = launches_per_step * args.steps
     prof = flce.LaunchProfiler(capacity=cap)
@@ -378,6 +377,8 @@ def run_ours(args, rank, world, local):
                      "launches_per_step": gemm_launches / args.steps if gemm_launches else None,
                      "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)"},
         "kernel_ms_per_step": {k: v["ms"] / args.steps for k, v in sorted(per_kind.items())},
+        # every launch of one untimed step, in order: (kind, device ms)
+        "launches_one_step": one_step,
         "gpu_launches": prof.count,
         "memory": {"workspace_mib": ws_bytes / 2 ** 20, "peak_extra_alloc_mib": peak_extra / 2 ** 20,
                    "logits_avoided_mib": wl.logits_bytes_bf16() / 2 ** 20},

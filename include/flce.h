@@ -221,6 +221,20 @@ flce_status flce_forward_backward_adamw(const flce_problem* p, const void* H, co
                                         float* adam_m, float* adam_v, void* w_out, const flce_adamw_hparams* hp,
                                         void* ws, size_t ws_bytes, void* stream);
 
+/* One AdamW step on n elements outside the LM-head call: the two-phase
+ * counterpart of flce_forward_backward_adamw (for example after
+ * flce_forward_backward, or for batches of more than one row chunk), with
+ * the same arithmetic as its fused epilogue. grad (fp32 [n], e.g. dW)
+ * updates w_master, adam_m and adam_v (fp32 [n]) in place; w_out (bf16 [n],
+ * may be NULL) receives the new weights rounded to nearest. hp is a device
+ * pointer as above. ws is any workspace of this library (256-byte aligned,
+ * at least 256 bytes): the step's constants and the status word go in its
+ * header, so it must not be in use by another call on another stream.
+ * grad, w_master, adam_m, adam_v 16-byte aligned and w_out 8-byte aligned,
+ * else FLCE_ERR_UNSUPPORTED. */
+flce_status flce_adamw_step(const flce_adamw_hparams* hp, const float* grad, float* w_master, float* adam_m,
+                            float* adam_v, void* w_out, int64_t n, void* ws, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* flce_status_string(flce_status s);
 
@@ -287,7 +301,8 @@ flce_status flce_forward_static_scratch(const flce_problem* p, const void* H, co
 #define FLCE_KERNEL_VOCAB_KEYS 11   /* average logits: column sums of H, their mean, W . mean */
 #define FLCE_KERNEL_VOCAB_SORT 12   /* stable radix sort of the averages, inverse order */
 #define FLCE_KERNEL_VOCAB_GATHER 13 /* W, bias and targets rearranged in the sorted order */
-#define FLCE_KERNEL_ADAMW_PREP 14   /* constants of the fused AdamW step */
+#define FLCE_KERNEL_ADAMW_PREP 14   /* constants of an AdamW step */
+#define FLCE_KERNEL_ADAMW_STEP 15   /* flce_adamw_step's elementwise update */
 flce_status flce_profile_set(void** events, int32_t* kinds, int32_t cap);
 int32_t flce_profile_count(void);
 

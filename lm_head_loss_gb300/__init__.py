@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     Status,
     declared_symbols,
     flce_forward,
+    flce_adamw_step,
     flce_backward_ex,
     flce_forward_backward,
     flce_forward_backward_adamw,

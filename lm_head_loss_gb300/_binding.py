@@ -92,6 +92,8 @@ def _load() -> ctypes.CDLL:
     lib.flce_forward_backward.restype = ctypes.c_int
     lib.flce_forward_backward_adamw.argtypes = [prob, vp, vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.flce_forward_backward_adamw.restype = ctypes.c_int
+    lib.flce_adamw_step.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp]
+    lib.flce_adamw_step.restype = ctypes.c_int
     lib.flce_get_device_status.argtypes = [vp, vp]
     lib.flce_get_device_status.restype = ctypes.c_int
     lib.flce_status_string.argtypes = [ctypes.c_int]
@@ -175,6 +177,11 @@ def flce_forward_backward_adamw(problem, H, W, y, grad_loss: float, lse, loss, d
         _addr(hparams), _addr(ws), nb, _stream(stream)))
 
 
+def flce_adamw_step(hparams, grad, w_master, adam_m, adam_v, w_out, n: int, ws, stream=None) -> Status:
+    return Status(lib.flce_adamw_step(_addr(hparams), _addr(grad), _addr(w_master), _addr(adam_m), _addr(adam_v),
+                                      _addr(w_out), int(n), _addr(ws), _stream(stream)))
+
+
 def flce_forward_ex(problem, reduction: int, H, W, bias, y, lse, loss, ws, ws_bytes: int | None = None,
                     stream=None) -> Status:
     nb = _nbytes(ws) if ws_bytes is None else ws_bytes
@@ -224,7 +231,8 @@ def flce_get_vocab_order(problem, ws, order, avg_logit=None, stream=None) -> Sta
 
 KERNEL_KINDS = {0: "gemm_lse", 1: "gemm_dz", 2: "gemm_dw", 3: "gemm_dh", 4: "prep", 5: "combine",
                 6: "finalize", 7: "filter_stats", 8: "gemm_bwd", 9: "dbias", 10: "set_scale",
-                11: "vocab_keys", 12: "vocab_sort", 13: "vocab_gather", 14: "adamw_prep"}
+                11: "vocab_keys", 12: "vocab_sort", 13: "vocab_gather", 14: "adamw_prep",
+                15: "adamw_step"}
 
 
 class LaunchProfiler:
@@ -252,6 +260,14 @@ class LaunchProfiler:
         self.count = int(lib.flce_profile_count())
         lib.flce_profile_set(None, None, 0)
         return False
+
+    def launches(self) -> list:
+        """(kind, device ms) of every recorded launch, in launch order."""
+        import torch
+        torch.cuda.synchronize()
+        return [(KERNEL_KINDS.get(self._kinds[i], str(self._kinds[i])),
+                 self.events[2 * i].elapsed_time(self.events[2 * i + 1]))
+                for i in range(min(self.count, self.capacity))]
 
     def summary(self) -> dict:
         import torch

@@ -64,6 +64,17 @@ enum EpiMode : int32_t { EPI_LSE = 0, EPI_DZ = 1, EPI_STORE = 2, EPI_REDUCE = 3,
 // beta1, beta2, eps.
 constexpr int kAdamwConsts = 6;
 
+// One AdamW update of one weight: c holds the kAdamwConsts step constants
+// (lr / (1 - beta1^t), 1 / sqrt(1 - beta2^t), 1 - lr * wd, beta1, beta2,
+// eps). Every rounding is spelled out, so the fused epilogue and the
+// standalone step give the same bits for the same gradient.
+__device__ __forceinline__ void adamw_update(const float* c, float g, float& p, float& m, float& v) {
+  m = fmaf(c[3], m, __fmul_rn(__fsub_rn(1.f, c[3]), g));
+  v = fmaf(c[4], v, __fmul_rn(__fmul_rn(__fsub_rn(1.f, c[4]), g), g));
+  const float q = __fdiv_rn(m, fmaf(sqrtf(v), c[1], c[5]));
+  p = fmaf(-c[0], q, __fmul_rn(p, c[2]));
+}
+
 // Device status bits (OR-ed into the workspace status word).
 constexpr uint32_t kDevBadTarget = 1u;
 constexpr uint32_t kDevTimeout = 2u;
@@ -138,6 +149,7 @@ struct GemmLaunch {
   GemmParams prob[kMaxProblems];
   int32_t n_probs;
   int32_t tile_end[kMaxProblems];
+  int32_t order_groups;        // pair kernel: TileOrder groups (1 = plain order)
 };
 static_assert(sizeof(GemmParams) % 128 == 0 && offsetof(GemmLaunch, prob) % 128 == 0,
               "problem parameters on 128-byte boundaries");
@@ -389,19 +401,34 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
     const float sc = __ldg(p.scale);
     if ((kModes & kModeAdamw) && p.mode == EPI_ADAMW) {
       // AdamW on the finished gradient tile (the FORGE explainer's fused
-      // optimizer): one thread per weight row, 16 columns at a time; rows go
-      // through out_rows when the vocabulary runs in sorted order.
-      const float step_size = __ldg(p.opt + 0), rs2 = __ldg(p.opt + 1), decay = __ldg(p.opt + 2);
-      const float b1 = __ldg(p.opt + 3), b2 = __ldg(p.opt + 4), eps = __ldg(p.opt + 5);
+      // optimizer): one thread per weight row, 32 columns at a time, rows
+      // through out_rows when the vocabulary runs in sorted order. The 24
+      // loads of a slice are issued before the accumulator is read, so the
+      // memory latency overlaps the TMEM read and the other warps' work.
+      float oc[kAdamwConsts];
+#pragma unroll
+      for (int i = 0; i < kAdamwConsts; ++i) oc[i] = __ldg(p.opt + i);
       const int srow = p.out_m0 + lrow;
       const bool row_ok = lrow < p.m_valid && srow < p.out_rows_n;
       const int64_t drow = row_ok ? (p.out_rows ? (int64_t)__ldg(p.out_rows + srow) : (int64_t)srow) : 0;
-      float* prow = p.out_ptr + drow * p.out_ld;
-      float* mrow = p.opt_m + drow * p.out_ld;
-      float* vrow = p.opt_v + drow * p.out_ld;
-      __nv_bfloat16* wrow = p.opt_w + drow * p.out_ld;
+      float* __restrict__ prow = p.out_ptr + drow * p.out_ld;
+      float* __restrict__ mrow = p.opt_m + drow * p.out_ld;
+      float* __restrict__ vrow = p.opt_v + drow * p.out_ld;
+      __nv_bfloat16* __restrict__ wrow = p.opt_w + drow * p.out_ld;
 #pragma unroll 1
       for (int c = 0; c < kBN; c += 32) {
+        const int c0 = nt * kBN + c;             // out_cols is a multiple of 8
+        float4 pv[8], mv[8], vv[8];
+        if (row_ok) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (c0 + 4 * j < p.out_cols) {
+              pv[j] = *reinterpret_cast<const float4*>(prow + c0 + 4 * j);
+              mv[j] = *reinterpret_cast<const float4*>(mrow + c0 + 4 * j);
+              vv[j] = *reinterpret_cast<const float4*>(vrow + c0 + 4 * j);
+            }
+          }
+        }
         float x[32];
         if (all_skipped) {
 #pragma unroll
@@ -414,51 +441,31 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
           for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * sc;
         }
         if (!row_ok) continue;
+        uint32_t wb[16];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c0 = nt * kBN + c + 16 * h;   // out_cols is a multiple of 8
-          float4 pv[4], mv[4], vv[4];
+        for (int j = 0; j < 8; ++j) {
+          float* pe = &pv[j].x;
+          float* me = &mv[j].x;
+          float* ve = &vv[j].x;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (c0 + 4 * j < p.out_cols) {
-              pv[j] = *reinterpret_cast<const float4*>(prow + c0 + 4 * j);
-              mv[j] = *reinterpret_cast<const float4*>(mrow + c0 + 4 * j);
-              vv[j] = *reinterpret_cast<const float4*>(vrow + c0 + 4 * j);
-            }
-          }
-          uint32_t wb[8];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float* pe = &pv[j].x;
-            float* me = &mv[j].x;
-            float* ve = &vv[j].x;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float g = x[16 * h + 4 * j + e];
-              const float m = fmaf(b1, me[e], (1.f - b1) * g);
-              const float v = fmaf(b2, ve[e], (1.f - b2) * g * g);
-              me[e] = m;
-              ve[e] = v;
-              pe[e] = pe[e] * decay - step_size * (m / (sqrtf(v) * rs2 + eps));
-            }
-            __nv_bfloat162 lo = __floats2bfloat162_rn(pe[0], pe[1]), hi = __floats2bfloat162_rn(pe[2], pe[3]);
-            wb[2 * j] = *reinterpret_cast<uint32_t*>(&lo);
-            wb[2 * j + 1] = *reinterpret_cast<uint32_t*>(&hi);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (c0 + 4 * j < p.out_cols) {
-              *reinterpret_cast<float4*>(prow + c0 + 4 * j) = pv[j];
-              *reinterpret_cast<float4*>(mrow + c0 + 4 * j) = mv[j];
-              *reinterpret_cast<float4*>(vrow + c0 + 4 * j) = vv[j];
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-            if (c0 + 8 * q < p.out_cols)
-              *reinterpret_cast<uint4*>(wrow + c0 + 8 * q) = make_uint4(wb[4 * q], wb[4 * q + 1], wb[4 * q + 2],
-                                                                        wb[4 * q + 3]);
+          for (int e = 0; e < 4; ++e) adamw_update(oc, x[4 * j + e], pe[e], me[e], ve[e]);
+          __nv_bfloat162 lo = __floats2bfloat162_rn(pe[0], pe[1]), hi = __floats2bfloat162_rn(pe[2], pe[3]);
+          wb[2 * j] = *reinterpret_cast<uint32_t*>(&lo);
+          wb[2 * j + 1] = *reinterpret_cast<uint32_t*>(&hi);
         }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (c0 + 4 * j < p.out_cols) {
+            *reinterpret_cast<float4*>(prow + c0 + 4 * j) = pv[j];
+            *reinterpret_cast<float4*>(mrow + c0 + 4 * j) = mv[j];
+            *reinterpret_cast<float4*>(vrow + c0 + 4 * j) = vv[j];
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (c0 + 8 * q < p.out_cols)
+            *reinterpret_cast<uint4*>(wrow + c0 + 8 * q) = make_uint4(wb[4 * q], wb[4 * q + 1], wb[4 * q + 2],
+                                                                      wb[4 * q + 3]);
       }
     } else if (p.out_rows) {
       // Row-mapped output (a vocabulary visited in sorted order writes dW

@@ -38,6 +38,27 @@ static_assert(pair_smem_bytes(kModesBackward) <= 232448 && pair_smem_bytes(kMode
               "shared memory of the pair kernel");
 static_assert((2 * kPairStagesLse + 5) * 8 + 8 <= kBarrierBytes, "barrier area of the pair kernel");
 
+// The tiles one pair handles, in the order it handles them. A pair takes
+// every stride-th tile from unit0. With groups > 1 the pairs are cut into
+// that many runs of consecutive pairs, and run k starts its list k/groups of
+// the way in: the problems of one launch then run side by side (the fused
+// optimizer's memory-heavy epilogues overlap the other problems' MMAs),
+// while neighbouring pairs still take neighbouring tiles and share operands
+// in L2. Every role of the pair walks the same order.
+struct TileOrder {
+  int unit0, stride, count, rot;
+  __device__ TileOrder(int unit0_, int stride_, int num_tiles, int groups)
+      : unit0(unit0_), stride(stride_), count(0), rot(0) {
+    count = unit0 < num_tiles ? (num_tiles - 1 - unit0) / stride + 1 : 0;
+    if (groups > 1 && count > 0) rot = (int)((int64_t)count * ((int64_t)unit0 * groups / stride) / groups);
+  }
+  __device__ int tile(int j) const {
+    int jj = j + rot;
+    if (jj >= count) jj -= count;
+    return unit0 + jj * stride;
+  }
+};
+
 // kSkip: some problem of the launch leaves out filtered k-blocks. Launches
 // without filtering use the kSkip = false instance, whose k-loops carry no
 // skip test at all. kModes: the epilogue set (kModesForward,
@@ -105,9 +126,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
       int32_t last_parity[kStg];
       for (int s = 0; s < kStg; ++s) last_parity[s] = -1;
       bool ok = true;
-      for (int t = unit0; t < num_tiles && ok; t += unit_stride) {
+      const TileOrder ord(unit0, unit_stride, num_tiles, L.order_groups);
+      for (int j = 0; j < ord.count && ok; ++j) {
         int pi, mt, nt;
-        const int tl = decode_tile(L, t, pi);
+        const int tl = decode_tile(L, ord.tile(j), pi);
         const GemmParams& p = L.prob[pi];
         const CUtensorMap* tmA = &L.tm_a[pi];
         const CUtensorMap* tmB = &L.tm_b[pi];
@@ -162,10 +184,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
       const uint32_t smem_base = ptx::smem_u32(smem);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
-      int i = 0;
-      for (int t = unit0; t < num_tiles && ok; t += unit_stride, ++i) {
+      const TileOrder ord(unit0, unit_stride, num_tiles, L.order_groups);
+      for (int i = 0; i < ord.count && ok; ++i) {
         int pi, mt, nt;
-        const int tl = decode_tile(L, t, pi);
+        const int tl = decode_tile(L, ord.tile(i), pi);
         const GemmParams& p = L.prob[pi];
         tile_coords(p, tl, 2, rank, mt, nt);
         const uint32_t idesc = ptx::idesc_bf16_f32(2 * kBM, kBN, p.a_mn != 0, p.b_mn != 0);
@@ -221,10 +243,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
     const int q = warp & 3;
     uint8_t* my_boxes = epi_smem + q * 2 * kEpiBoxBytes;
     uint32_t ebuf = 0;
-    int i = 0;
-    for (int t = unit0; t < num_tiles; t += unit_stride, ++i) {
+    const TileOrder ord(unit0, unit_stride, num_tiles, L.order_groups);
+    for (int i = 0; i < ord.count; ++i) {
       int pi, mt, nt;
-      const int tl = decode_tile(L, t, pi);
+      const int tl = decode_tile(L, ord.tile(i), pi);
       const GemmParams& p = L.prob[pi];
       const CUtensorMap* tmOut = &L.tm_out[pi];
       tile_coords(p, tl, 2, rank, mt, nt);

@@ -21,7 +21,7 @@ def test_library_exports_every_declared_symbol():
                              "flce_get_device_status", "flce_status_string", "flce_get_filter_stats",
                              "flce_profile_set", "flce_profile_count", "flce_forward_static_scratch",
                              "flce_forward_ex", "flce_backward_ex", "flce_forward_workspace_bytes",
-                             "flce_get_vocab_order", "flce_forward_backward_adamw"}
+                             "flce_get_vocab_order", "flce_forward_backward_adamw", "flce_adamw_step"}
     out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
     for name in declared:
@@ -113,6 +113,16 @@ def test_fused_adamw_argument_checks():
     assert call(prob=many, n=flce.flce_workspace_bytes(many)) == Status.ERR_UNSUPPORTED
     none = flce.make_problem(0, 64, 100)
     assert call(prob=none, n=flce.flce_workspace_bytes(none)) == Status.ERR_UNSUPPORTED
+
+
+def test_adamw_step_argument_checks():
+    st = flce.flce_adamw_step
+    assert st(None, FAKE, FAKE, FAKE, FAKE, None, 10, FAKE, 0) == Status.ERR_INVALID_ARGUMENT
+    assert st(FAKE, FAKE, FAKE, FAKE, FAKE, None, -1, FAKE, 0) == Status.ERR_INVALID_ARGUMENT
+    assert st(FAKE, FAKE, FAKE, FAKE, FAKE, None, 10, None, 0) == Status.ERR_INVALID_ARGUMENT
+    assert st(FAKE, FAKE, FAKE, FAKE, FAKE, None, 10, FAKE + 64, 0) == Status.ERR_INVALID_ARGUMENT
+    assert st(FAKE, FAKE + 4, FAKE, FAKE, FAKE, None, 10, FAKE, 0) == Status.ERR_UNSUPPORTED
+    assert st(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, 10, FAKE, 0) == Status.ERR_UNSUPPORTED
 
 
 def test_workspace_bytes_rejects_bad_problems():

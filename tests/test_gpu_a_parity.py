@@ -46,6 +46,18 @@ def test_ragged_shapes(n, d, v):
     print((n, d, v), e)
 
 
+@pytest.mark.parametrize("n,d,v", [(200, 64, 1_000_003), (300, 16384, 3000)])
+def test_extreme_shapes(n, d, v):
+    # A vocabulary of a million ids (3907 logit tiles, over a hundred
+    # vocabulary chunks) and a hidden size of 16384 (256 k-blocks per tile).
+    inp = small_inputs(n, d, v, seed=n + v, targets="zipf", ignore=0.05)
+    ref = oracle_full(inp)
+    got = gpu_fwd_bwd(inp)
+    assert got["status"] == flce.Status.OK
+    e = assert_parity(got, ref)
+    print((n, d, v), e)
+
+
 def test_several_row_and_vocab_chunks():
     # 2 row chunks (8192 + 384 rows) x 3 vocabulary chunks (8192 + 8192 + 100).
     inp = small_inputs(8192 + 384, 64, 2 * 8192 + 100, seed=3, targets="zipf", ignore=0.1)

@@ -147,3 +147,48 @@ def test_fused_adamw_head_three_steps():
     assert np.all(np.abs(got - p) <= 2 * tol), float(np.max(np.abs(got - p) / tol))
     assert float(np.median(np.abs(p - p0))) > 20 * float(np.median(tol))
     assert flce.device_status(head.workspace) == flce.Status.OK
+
+
+def test_standalone_adamw_step_matches_the_oracle():
+    n = 1_000_003                      # a tail of 3 after the 4-wide part
+    rng = np.random.default_rng(99)
+    p0 = rng.standard_normal(n).astype(np.float32)
+    g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    m0 = (rng.standard_normal(n) * 1e-4).astype(np.float32)
+    v0 = (rng.random(n) * 1e-6 + 1e-8).astype(np.float32)
+    dev = torch.device("cuda")
+    tp, tm, tv, tg = (torch.from_numpy(a.copy()).to(dev) for a in (p0, m0, v0, g))
+    w = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    hp = flce.adamw_hparams(HP["lr"], 5, (HP["beta1"], HP["beta2"]), HP["eps"], HP["weight_decay"], dev)
+    ws = torch.zeros(1024, dtype=torch.uint8, device=dev)     # status word clear
+    assert flce.flce_adamw_step(hp, tg, tp, tm, tv, w, n, ws) == flce.Status.OK
+    assert flce.flce_get_device_status(ws) == flce.Status.OK
+    p, m, v = oracle.adamw_step(p0, g, m0, v0, 5, **HP)
+    gp, gm, gv = tp.cpu().numpy(), tm.cpu().numpy(), tv.cpu().numpy()
+    # fp32 arithmetic on fp32 inputs: a few roundings of each term.
+    b1, b2 = HP["beta1"], HP["beta2"]
+    assert np.all(np.abs(gm - m) <= 1e-6 * (b1 * np.abs(m0) + (1 - b1) * np.abs(g)) + 1e-15)
+    assert np.all(np.abs(gv - v) <= 1e-6 * (b2 * v0 + (1 - b2) * g * g) + 1e-20)
+    assert np.all(np.abs(gp - p) <= 1e-5 * HP["lr"] + 2.0 ** -22 * np.abs(p))
+    assert np.array_equal(w.view(torch.int16).cpu().numpy().view(np.uint16),
+                          synth.f64_to_bf16_bits(gp.astype(np.float64)))
+
+
+def test_fused_step_equals_gradient_then_standalone_step_bit_for_bit():
+    # The fused epilogue applies the same update to the same fp32 gradient
+    # the two-phase path stores as dW, so both give identical bits.
+    inp = small_inputs(2000, 128, 6000, seed=100, targets="zipf", ignore=0.1)
+    master, m, v = _state(inp, 9)
+    fused = _gpu_step(inp, master, m, v, 6)
+    H, W, y = to_device(inp)
+    dev = H.device
+    tm, tmm, tv = (torch.from_numpy(a.copy()).to(dev) for a in (master, m, v))
+    w_out = torch.empty(W.shape, dtype=torch.bfloat16, device=dev)
+    hp = flce.adamw_hparams(HP["lr"], 6, (HP["beta1"], HP["beta2"]), HP["eps"], HP["weight_decay"], dev)
+    ws = flce.Workspace(dev)
+    loss, lse, dH, dW = flce.forward_backward(H, W, y, workspace=ws)
+    assert flce.flce_adamw_step(hp, dW, tm, tmm, tv, w_out, W.numel(), ws.buf) == flce.Status.OK
+    assert np.array_equal(tm.cpu().numpy(), fused["master"])
+    assert np.array_equal(tmm.cpu().numpy(), fused["m"]) and np.array_equal(tv.cpu().numpy(), fused["v"])
+    assert np.array_equal(w_out.view(torch.int16).cpu().numpy().view(np.uint16), fused["w_out"])
+    assert np.array_equal(dH.cpu().numpy(), fused["dH"])
