@@ -51,14 +51,22 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
+// Longest time one try_wait may suspend the thread before it re-tests the
+// phase. Without a hint the suspension lasts a system-dependent time, and
+// measured on GB300 the GEMM's hand-offs between its warps (accumulator
+// full/empty, shared-memory stages) then ran late: a step of the Gravity
+// head took 12.5 ms against 11.8 ms with this hint, and launches whose tiles
+// were all filtered out cost 80 instead of 50 us.
+constexpr uint32_t kWaitHintNs = 128;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kWaitHintNs)
       : "memory");
   return ok != 0;
 }

@@ -235,6 +235,9 @@ WORKLOADS: dict[str, Workload] = {
     "gemma2_2b_head_prior": Workload("gemma2_2b_head_prior", 8192, 2304, 256000, 9.0, "top16", 0.0,
                                      description="Gemma-2-2B-shaped head whose rows share a component, "
                                                  "so tokens carry a common logit prior", h_shared=2.0),
+    "gemma2_2b_head_prior_v65536": Workload("gemma2_2b_head_prior_v65536", 8192, 2304, 65536, 9.0, "top16", 0.0,
+                                            description="the same with the vocabulary cut to 65536, for "
+                                                        "profiler captures", h_shared=2.0),
 }
 
 
