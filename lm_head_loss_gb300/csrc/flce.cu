@@ -704,9 +704,21 @@ static bool backward_grouping() {
   return on;
 }
 
+// FLCE_VOCAB_CHUNK=<ids> (a multiple of 256, for comparisons) overrides the
+// model's choice, within the workspace's chunk size.
+static int vocab_chunk_override() {
+  static const int vc = [] {
+    const char* e = std::getenv("FLCE_VOCAB_CHUNK");
+    const int v = e ? std::atoi(e) : 0;
+    return v >= 256 && v % 256 == 0 ? v : 0;
+  }();
+  return vc;
+}
+
 static void choose_backward_chunk(Plan& pl, const flce_problem& p, int sms) {
   const int cluster = backward_mode(p) == GEMM_CTA1 ? 1 : 2;
   pl.vcu = choose_vocab_chunk(p, pl.nc, pl.vc, std::max(1, sms / cluster), cluster);
+  if (vocab_chunk_override()) pl.vcu = std::min(pl.vc, vocab_chunk_override());
   pl.v_chunks = (int)ceil_div(p.vocab, pl.vcu);
 }
 

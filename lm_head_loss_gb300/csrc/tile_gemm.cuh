@@ -219,7 +219,9 @@ struct AccRelease {
   uint64_t* local;          // barrier in this CTA, or
   uint32_t cluster_addr;    // its shared::cluster address in the MMA-issuing CTA
   bool remote;
+  bool none = false;        // a tile written without an accumulator: nothing to release
   __device__ __forceinline__ void arrive() const {
+    if (none) return;
     if (remote)
       ptx::mbar_arrive_cluster(cluster_addr);
     else

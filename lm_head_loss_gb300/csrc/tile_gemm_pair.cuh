@@ -185,13 +185,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       const TileOrder ord(unit0, unit_stride, num_tiles, L.order_groups);
-      for (int i = 0; i < ord.count && ok; ++i) {
+      int i = 0;                                      // accumulators used so far
+      for (int j = 0; j < ord.count && ok; ++j) {
         int pi, mt, nt;
-        const int tl = decode_tile(L, ord.tile(i), pi);
+        const int tl = decode_tile(L, ord.tile(j), pi);
         const GemmParams& p = L.prob[pi];
         tile_coords(p, tl, 2, rank, mt, nt);
+        const bool may_skip = kSkip && p.skip_by_flags != 0;
+        const uint64_t keep = may_skip ? tile_keep(p, mt, 2) : ~0ull;   // mt: the even CTA's m-tile
+        // A tile with every k-block filtered out needs no accumulator: the
+        // epilogue writes it without reading TMEM, and both sides skip the
+        // hand-off for it.
+        if (kSkip && may_skip && keep == 0ull) continue;
         const uint32_t idesc = ptx::idesc_bf16_f32(2 * kBM, kBN, p.a_mn != 0, p.b_mn != 0);
         const uint32_t buf = i & 1, use = i >> 1;
+        ++i;
         if (!ptx::mbar_wait_bounded(&acc_empty[buf], (use & 1u) ^ 1u, wait_limit_ns, abort_flag)) {
           record_timeout(status, abort_flag);
           ok = false;
@@ -201,8 +209,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
         const uint32_t d_tmem = tmem_base + buf * kBN;
         uint32_t accumulate = 0;
         const bool a_mn = p.a_mn != 0, b_mn = p.b_mn != 0;
-        const bool may_skip = kSkip && p.skip_by_flags != 0;
-        const uint64_t keep = may_skip ? tile_keep(p, mt, 2) : ~0ull;   // mt: the even CTA's m-tile
         const int k_blocks = p.k_blocks;
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (kSkip && may_skip && kblock_dropped(p, keep, kb)) continue;
@@ -244,20 +250,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
     uint8_t* my_boxes = epi_smem + q * 2 * kEpiBoxBytes;
     uint32_t ebuf = 0;
     const TileOrder ord(unit0, unit_stride, num_tiles, L.order_groups);
-    for (int i = 0; i < ord.count; ++i) {
+    int i = 0;                                        // accumulators used so far
+    for (int j = 0; j < ord.count; ++j) {
       int pi, mt, nt;
-      const int tl = decode_tile(L, ord.tile(i), pi);
+      const int tl = decode_tile(L, ord.tile(j), pi);
       const GemmParams& p = L.prob[pi];
       const CUtensorMap* tmOut = &L.tm_out[pi];
       tile_coords(p, tl, 2, rank, mt, nt);
-      const uint32_t buf = i & 1, use = i >> 1;
-      if (!ptx::mbar_wait_bounded(&acc_full[buf], use & 1u, wait_limit_ns, abort_flag)) {
-        record_timeout(status, abort_flag);
-        break;
+      // A tile with no accumulator (see the MMA issuer) is written without
+      // waiting for one and releases nothing.
+      const bool no_acc = kSkip && p.skip_by_flags != 0 && tile_keep(p, mt - rank, 2) == 0ull;
+      uint32_t buf = 0;
+      if (!no_acc) {
+        buf = i & 1;
+        const uint32_t use = i >> 1;
+        ++i;
+        if (!ptx::mbar_wait_bounded(&acc_full[buf], use & 1u, wait_limit_ns, abort_flag)) {
+          record_timeout(status, abort_flag);
+          break;
+        }
+        ptx::tc_fence_after();
       }
-      ptx::tc_fence_after();
       const uint32_t taddr = tmem_base + buf * kBN + ((uint32_t)(q * 32) << 16);
-      const AccRelease rel{&acc_empty[buf], ptx::map_to_rank(&acc_empty[buf], 0), !leader};
+      const AccRelease rel{&acc_empty[buf], ptx::map_to_rank(&acc_empty[buf], 0), !leader, no_acc};
       epilogue_tile<kModes>(p, tmOut, mt, nt, taddr, q, lane, my_boxes, ebuf, rel, 2);
     }
     if (lane == 0) ptx::bulk_wait_group<0>();

@@ -192,3 +192,56 @@ def test_fused_step_equals_gradient_then_standalone_step_bit_for_bit():
     assert np.array_equal(tmm.cpu().numpy(), fused["m"]) and np.array_equal(tv.cpu().numpy(), fused["v"])
     assert np.array_equal(w_out.view(torch.int16).cpu().numpy().view(np.uint16), fused["w_out"])
     assert np.array_equal(dH.cpu().numpy(), fused["dH"])
+
+
+def test_fused_step_in_a_cuda_graph_reads_each_replays_hyperparameters():
+    # The hyper-parameters live in device memory, so one captured graph serves
+    # every step: replays with new values written into the same buffer match
+    # eager calls with those values, bit for bit.
+    inp = small_inputs(1200, 128, 5000, seed=101, targets="zipf", ignore=0.05)
+    master, m, v = _state(inp, 10)
+    H, W, y = to_device(inp)
+    dev = H.device
+    n, d, vv = H.shape[0], H.shape[1], W.shape[0]
+    prob = flce.make_problem(n, d, vv)
+    ws = torch.empty(flce.flce_workspace_bytes(prob), dtype=torch.uint8, device=dev)
+    lse, loss = torch.empty(n, device=dev), torch.empty((), device=dev)
+    dH = torch.empty(n, d, device=dev)
+    w_out = torch.empty(W.shape, dtype=torch.bfloat16, device=dev)
+    state = [torch.from_numpy(a.copy()).to(dev) for a in (master, m, v)]
+    hp = flce.adamw_hparams(HP["lr"], 1, (HP["beta1"], HP["beta2"]), HP["eps"], HP["weight_decay"], dev)
+
+    def call(stream=None):
+        return flce.flce_forward_backward_adamw(prob, H, W, y, 1.0, lse, loss, dH, *state, w_out, hp, ws,
+                                                stream=stream)
+
+    def set_step(t, lr):
+        hp.copy_(flce.adamw_hparams(lr, t, (HP["beta1"], HP["beta2"]), HP["eps"], HP["weight_decay"], dev))
+
+    # Eager reference: two steps with different step counts and learning rates.
+    assert call() == flce.Status.OK                      # also sets the device up before capture
+    for t, a in zip(state, (master, m, v)):
+        t.copy_(torch.from_numpy(a))
+    eager = []
+    for t, lr in ((3, 1e-3), (4, 5e-4)):
+        set_step(t, lr)
+        assert call() == flce.Status.OK
+        eager.append([x.clone() for x in state] + [w_out.clone(), dH.clone(), loss.clone()])
+    # The same two steps as replays of one graph.
+    for t, a in zip(state, (master, m, v)):
+        t.copy_(torch.from_numpy(a))
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    set_step(1, 0.0)
+    torch.cuda.synchronize()
+    saved = [x.clone() for x in state]
+    with torch.cuda.graph(graph, stream=side):
+        assert call(stream=side) == flce.Status.OK
+    for x, s0 in zip(state, saved):                       # capture runs nothing; restore anyway
+        x.copy_(s0)
+    for (t, lr), ref in zip(((3, 1e-3), (4, 5e-4)), eager):
+        set_step(t, lr)
+        graph.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(state + [w_out, dH, loss], ref):
+            assert torch.equal(a, b)
