@@ -34,7 +34,9 @@
  *    word, per-tile LSE partials, the per-row LSE when the caller passes no
  *    lse buffer, and two bf16 staging buffers for bounded chunks of dZ
  *    (at most 8192 x 10240 each). Its size grows with N + V, never with
- *    N * V.
+ *    N * V (the vocabulary-sorting and ignored-row-compaction flags below add
+ *    a copy of W and of the valid rows). The forward-only calls need only
+ *    flce_forward_workspace_bytes(p) bytes of it.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and the call returns without synchronising. Errors found on the
  *    host are returned before anything is launched. Errors found by the GPU
