@@ -91,14 +91,20 @@ def rank_seed(base_seed: int, rank: int) -> int:
 
 
 def kernel_sources_sha256() -> str:
-    """Digest of the CUDA sources: a recorded DRAM capture is only used while it matches."""
+    """Digest of the CUDA sources' code (comments and blank space removed): a
+    recorded DRAM capture is only used while it matches."""
     import hashlib
+    import re
     csrc = os.path.join(ROOT, "lm_head_loss_gb300", "csrc")
     h = hashlib.sha256()
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", "", text)
+            code = "\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip())
+            h.update(name.encode() + b"\0" + code.encode())
     return h.hexdigest()
 
 

@@ -7,7 +7,7 @@
 //   warp 1      MMA issuer: one lane issues tcgen05.mma (M=128, N=256, K=16)
 //               into one of two 256-column fp32 TMEM accumulators;
 //   warps 2..5  epilogue: tcgen05.ld the 128x256 accumulator (one thread per
-//               row) and apply one of four epilogues:
+//               row) and apply one of five epilogues:
 //     EPI_LSE    per-row max and sum of exp over the tile's 256 vocabulary
 //                columns, written as one (max, sum) partial per row and tile,
 //                plus the target logit when the row's target falls in the

@@ -2,9 +2,10 @@
 // M = 256 (128 rows in each CTA of a 2-CTA cluster) and N = 256.
 //
 // Each CTA streams its own 128x64 A box and its half (128 of the 256
-// columns) of the B tile into a 6-stage ring; the pair's tensor cores share
-// the two B halves, so every SM moves 32 KiB per 64-deep k-block instead of
-// 48 KiB, and more stages fit in shared memory. The even CTA's producer
+// columns) of the B tile into a 6-stage ring (7 for the forward's instance,
+// which needs no store boxes); the pair's tensor cores share the two B
+// halves, so every SM moves 32 KiB per 64-deep k-block instead of 48 KiB,
+// and more stages fit in shared memory. The even CTA's producer
 // expects the bytes of both CTAs on its full barrier, the odd CTA's TMA
 // loads complete on that barrier, and the even CTA's single MMA thread
 // issues the MMAs and releases both CTAs' stages and accumulators with
@@ -14,7 +15,8 @@
 // With gradient filtering the pair leaves out a k-block only when both CTAs'
 // tiles skip it: the dW mask stays 128 rows x 256 vocabulary ids (both
 // halves of a dW group read the same dZ tile), the dH mask becomes 256 rows
-// x 256 ids (the two halves are two row tiles).
+// x 256 ids (the two halves are two row tiles). A tile whose k-blocks are
+// all left out takes no accumulator at all.
 #pragma once
 
 #include "tile_gemm.cuh"
