@@ -66,7 +66,8 @@ def _check_order(got, H64, W64, y, bias=None, ignore_index=-100):
 
 
 @pytest.mark.parametrize("n,d,v,with_bias", [(300, 64, 1000, False), (1000, 136, 5000, True),
-                                             (8192 + 300, 64, 2 * 8192 + 100, False), (5, 8, 3, True)])
+                                             (8192 + 300, 64, 2 * 8192 + 100, False), (5, 8, 3, True),
+                                             (8192 + 300, 64, 9000, True)])
 def test_sorted_backward_matches_the_unsorted_oracle(n, d, v, with_bias):
     inp = small_inputs(n, d, v, seed=70 + n, targets="zipf", ignore=0.1)
     bias = np.random.default_rng(n).standard_normal(v) * 0.5 if with_bias else None

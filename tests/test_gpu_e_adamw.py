@@ -245,3 +245,30 @@ def test_fused_step_in_a_cuda_graph_reads_each_replays_hyperparameters():
         torch.cuda.synchronize()
         for a, b in zip(state + [w_out, dH, loss], ref):
             assert torch.equal(a, b)
+
+
+def test_fused_step_with_filter_equals_filtered_gradient_then_step():
+    # With the filter on, tiles whose gradient was left out reach the fused
+    # update as exact zeros, as they reach a stored dW: the two paths agree
+    # bit for bit (the filtered gradient itself is checked against the
+    # oracle's tile mask in the parity tests).
+    wl = synth.Workload("peaky_filter", 512, 64, 262144, 900.0, "top16", 0.0)
+    inp = synth.make_inputs(wl, seed=12)
+    master, m, v = _state(inp, 11)
+    H, W, y = to_device(inp)
+    dev = H.device
+    eps = 2.0 ** -12
+    hp = flce.adamw_hparams(HP["lr"], 2, (HP["beta1"], HP["beta2"]), HP["eps"], HP["weight_decay"], dev)
+    fused = [torch.from_numpy(a.copy()).to(dev) for a in (master, m, v)]
+    w_f = torch.empty(W.shape, dtype=torch.bfloat16, device=dev)
+    ws = flce.Workspace(dev)
+    loss_f, _, dH_f = flce.forward_backward_adamw(H, W, y, *fused, w_f, hp, filter_eps=eps, workspace=ws)
+    skipped = flce.flce_get_filter_stats(ws.buf)
+    assert skipped > 0.5
+    two = [torch.from_numpy(a.copy()).to(dev) for a in (master, m, v)]
+    w_t = torch.empty(W.shape, dtype=torch.bfloat16, device=dev)
+    ws2 = flce.Workspace(dev)
+    loss_t, _, dH_t, dW = flce.forward_backward(H, W, y, filter_eps=eps, workspace=ws2)
+    assert flce.flce_adamw_step(hp, dW, *two, w_t, W.numel(), ws2.buf) == flce.Status.OK
+    for a, b in zip(fused + [w_f, dH_f, loss_f], two + [w_t, dH_t, loss_t]):
+        assert torch.equal(a, b)
