@@ -8,13 +8,20 @@
 //     GEMM  EPI_LSE           logits tile -> per-tile (max, sum-exp) + target logit
 //     lse_combine             fixed-order merge of the tile partials -> LSE, row losses
 //   finalize                  fixed-order fp64 sum -> mean loss, scale = g / count
-//   per row chunk, per vocabulary chunk (<= 8192 ids):
+//   per row chunk, per vocabulary chunk (<= 10240 ids, picked by a makespan
+//   model; dW and dH of chunk c run in one launch with EPI_DZ of chunk c+1):
 //     GEMM  EPI_DZ            recomputed logits -> bf16 G = softmax - onehot -> staging
 //     GEMM  dW chunk          dW[v-chunk] (=|+=) scale * staging^T H[row chunk]
 //     GEMM  dH chunk          dH[row chunk] (=|+=) scale * staging W[v-chunk]
 // The first contribution to an output tile is a plain store and later ones a
 // TMA reduce-add, so no output needs zeroing and every sum runs in launch
 // order: results are bit-reproducible.
+//
+// Options around that schedule: a bias and mean / sum / none reductions
+// (flce_forward_ex, flce_backward_ex), the gradient filter's per-tile flags
+// and keep masks, ignored-row compaction, vocabulary sorting
+// (vocab_sort.cuh), and AdamW on W applied in the dW epilogue
+// (flce_forward_backward_adamw) or after it (flce_adamw_step).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
