@@ -103,7 +103,7 @@ def kernel_sources_sha256() -> str:
                 text = f.read()
             text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
             text = re.sub(r"//[^\n]*", "", text)
-            code = "\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip())
+            code = " ".join(text.split())
             h.update(name.encode() + b"\0" + code.encode())
     return h.hexdigest()
 
