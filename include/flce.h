@@ -35,7 +35,8 @@
  *    lse buffer, and two bf16 staging buffers for bounded chunks of dZ
  *    (at most 8192 x 10240 each). Its size grows with N + V, never with
  *    N * V (the vocabulary-sorting and ignored-row-compaction flags below add
- *    a copy of W and of the valid rows). The forward-only calls need only
+ *    a copy of W and of the valid rows; problems of more than 8192 rows also
+ *    hold one vocabulary chunk's fp32 dW for flce_forward_backward_adamw). The forward-only calls need only
  *    flce_forward_workspace_bytes(p) bytes of it.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and the call returns without synchronising. Errors found on the
@@ -212,8 +213,12 @@ typedef struct {
  *     the master weights and moments unchanged and make
  *     flce_get_device_status report FLCE_ERR_INVALID_ARGUMENT.
  *   Other arguments and results as flce_forward_backward (dH, LSE, loss).
- *   The rows must fit one 8192-row chunk (n_rows in 1..8192), so each dW
- *   tile is complete after one contraction; otherwise FLCE_ERR_UNSUPPORTED.
+ *   With n_rows <= 8192 (one row chunk) each dW tile is complete after one
+ *   contraction and is applied straight from the accumulator. With more rows
+ *   the vocabulary chunks run one after another, each chunk's dW is summed
+ *   over the row chunks in a Vc x D fp32 buffer of the workspace, and its
+ *   AdamW step runs as soon as it is complete: no more than one chunk's
+ *   gradient (at most 10240 x D) exists at a time. n_rows must be >= 1.
  *   The gradient of a tile is final only when the whole batch is in it: a
  *   data-parallel run that must all-reduce dW cannot use this entry point
  *   (the page says the same of FORGE). Combines with filtering, sorting and
@@ -225,8 +230,8 @@ flce_status flce_forward_backward_adamw(const flce_problem* p, const void* H, co
 
 /* One AdamW step on n elements outside the LM-head call: the two-phase
  * counterpart of flce_forward_backward_adamw (for example after
- * flce_forward_backward, or for batches of more than one row chunk), with
- * the same arithmetic as its fused epilogue. grad (fp32 [n], e.g. dW)
+ * flce_forward_backward), with the same arithmetic as its fused epilogue,
+ * so the two give the same bits for the same gradient. grad (fp32 [n], e.g. dW)
  * updates w_master, adam_m and adam_v (fp32 [n]) in place; w_out (bf16 [n],
  * may be NULL) receives the new weights rounded to nearest. hp is a device
  * pointer as above. ws is any workspace of this library (256-byte aligned,

@@ -254,6 +254,40 @@ __global__ void __launch_bounds__(256) adamw_step_kernel(const WsHeader* __restr
   }
 }
 
+// The fused optimizer's step for one vocabulary chunk of a batch of several
+// row chunks: part [cols][d] is the chunk's summed dW (chunk-local rows in
+// visiting order); row i updates the weights of id v0 + i, or of
+// id order[v0 + i] when the vocabulary runs in sorted order. Four weights per
+// thread (d is a multiple of 8), adamw_update as everywhere else.
+__global__ void __launch_bounds__(256) adamw_rows_kernel(const WsHeader* __restrict__ hdr,
+                                                         const float* __restrict__ part, int cols, int d,
+                                                         const int32_t* __restrict__ order, int64_t v0,
+                                                         float* __restrict__ p, float* __restrict__ m,
+                                                         float* __restrict__ v, __nv_bfloat16* __restrict__ w) {
+  float c[kAdamwConsts];
+  for (int i = 0; i < kAdamwConsts; ++i) c[i] = hdr->opt[i];
+  const int q = d / 4;
+  const int64_t n4 = (int64_t)cols * q;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const int64_t row = i / q, k = i % q;
+    const int64_t id = order ? (int64_t)__ldg(order + v0 + row) : v0 + row;
+    const int64_t e = id * q + k;
+    const float4 g4 = reinterpret_cast<const float4*>(part)[i];
+    float4 p4 = reinterpret_cast<float4*>(p)[e], m4 = reinterpret_cast<float4*>(m)[e],
+           v4 = reinterpret_cast<float4*>(v)[e];
+    adamw_update(c, g4.x, p4.x, m4.x, v4.x);
+    adamw_update(c, g4.y, p4.y, m4.y, v4.y);
+    adamw_update(c, g4.z, p4.z, m4.z, v4.z);
+    adamw_update(c, g4.w, p4.w, m4.w, v4.w);
+    reinterpret_cast<float4*>(p)[e] = p4;
+    reinterpret_cast<float4*>(m)[e] = m4;
+    reinterpret_cast<float4*>(v)[e] = v4;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(p4.x, p4.y), hi = __floats2bfloat162_rn(p4.z, p4.w);
+    reinterpret_cast<uint2*>(w)[e] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  }
+}
+
 // d(bias) of one staging chunk: out[dst(c)] (=|+=) scale * sum over the
 // chunk's rows of G[r][c], with dst(c) = v0 + c, or col_map[v0 + c] when the
 // vocabulary runs in sorted order. A block covers 32 columns; thread (c, g)
@@ -415,6 +449,7 @@ struct Plan {
   int n_vtiles;          // ceil(V / 256)
   int row_chunks, v_chunks;
   size_t off_pm, off_ps, off_zy, off_lse, off_bsum, off_flags[2], off_keep[2], off_stage[2];
+  size_t off_opt_part;   // fused optimizer, several row chunks: one chunk's dW [Vc][D] fp32 (0 = none)
   // vocabulary sorting (FLCE_FLAG_SORT_VOCAB only)
   size_t off_hpart, off_hmean, off_avg, off_keys[2], off_ids[2], off_inv, off_hist, off_bias_s, off_ys, off_wsort;
   // ignored-row compaction (FLCE_FLAG_COMPACT_IGNORED only)
@@ -456,6 +491,11 @@ static Plan make_plan_rows(const flce_problem& p, int nc) {
   for (int b = 0; b < 2; ++b) {
     pl.off_stage[b] = off;
     off = align_up(off + (size_t)pl.nc * pl.vc * 2, 1024);
+  }
+  pl.off_opt_part = 0;
+  if (pl.row_chunks > 1) {
+    pl.off_opt_part = off;
+    off = align_up(off + (size_t)pl.vc * p.hidden * 4, 1024);
   }
   if (p.flags & FLCE_FLAG_SORT_VOCAB) {
     // Sizes grow with N and V only, so the plan of a compacted problem (fewer
@@ -807,6 +847,7 @@ static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
 
 struct Maps {
   CUtensorMap h_k, w_k, w_k_half, h_mn, w_mn, dh, dw;
+  CUtensorMap opt_part;   // the fused optimizer's Vc x D dW buffer (several row chunks only)
   CUtensorMap s_store[2], s_k[2], s_mn[2];   // one set per staging buffer
 };
 
@@ -897,8 +938,23 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
   const int filter = p.filter_eps > 0.f ? 1 : 0;
   const int d_tiles = (int)ceil_div(p.hidden, kBN);
   const int items = pl.row_chunks * pl.v_chunks;
+  // Items run row-chunk-major, except with the fused optimizer over several
+  // row chunks: then vocabulary-chunk-major, so that a chunk's dW is complete
+  // (summed over the row chunks in a Vc x D buffer) before the next chunk's
+  // starts, and its AdamW step runs right after.
+  const bool vocab_major = opt && pl.row_chunks > 1;
+  auto item_rc_vi = [&](int s, int& rc, int& vi) {
+    if (vocab_major) {
+      rc = s % pl.row_chunks;
+      vi = s / pl.row_chunks;
+    } else {
+      rc = s / pl.v_chunks;
+      vi = s % pl.v_chunks;
+    }
+  };
   auto item_geom = [&](int s, int64_t& r0, int& rows, int64_t& v0, int& cols) {
-    const int rc = s / pl.v_chunks, vi = s % pl.v_chunks;
+    int rc, vi;
+    item_rc_vi(s, rc, vi);
     r0 = (int64_t)rc * pl.nc;
     rows = (int)std::min<int64_t>(pl.nc, p.n_rows - r0);
     v0 = (int64_t)vi * pl.vcu;
@@ -936,7 +992,8 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     int64_t r0, v0;
     int rows, cols;
     item_geom(s, r0, rows, v0, cols);
-    const int rc = s / pl.v_chunks;
+    int rc, vi;
+    item_rc_vi(s, rc, vi);
     const __nv_bfloat16* stage = reinterpret_cast<const __nv_bfloat16*>(ws + pl.off_stage[s & 1]);
     ProfScope prof(FLCE_KERNEL_DBIAS, st);
     dbias_chunk_kernel<<<(int)ceil_div(cols, 32), dim3(32, 8), 0, st>>>(stage, pl.vcu, rows, cols, &hdr->scale,
@@ -969,7 +1026,8 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     int64_t r0, v0;
     int rows, cols;
     item_geom(s, r0, rows, v0, cols);
-    const int rc = s / pl.v_chunks, vi = s % pl.v_chunks;
+    int rc, vi;
+    item_rc_vi(s, rc, vi);
     const uint64_t* keep = reinterpret_cast<const uint64_t*>(ws + pl.off_keep[b]);
     Group g(gm);
     // dW[v0 : v0+cols, :] (=|+=) scale * staging^T * H[r0 : r0+rows, :]
@@ -995,7 +1053,8 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
       dw.out_cols = (int32_t)p.hidden;
       dw.out_rows_n = (int32_t)p.vocab;
     }
-    if (opt) {
+    const CUtensorMap* dw_map = &mp.dw;
+    if (opt && !vocab_major) {
       // One row chunk: each dW tile is complete after this contraction.
       dw.mode = EPI_ADAMW;
       dw.out_ptr = opt->master;
@@ -1003,8 +1062,15 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
       dw.opt_m = opt->m;
       dw.opt_v = opt->v;
       dw.opt_w = opt->w_out;
+    } else if (opt) {
+      // Several row chunks: the chunk's dW is summed in the Vc x D buffer
+      // (chunk-local rows, in the order the vocabulary is visited) and the
+      // AdamW step follows the last row chunk (adamw_rows_kernel).
+      dw.out_rows = nullptr;
+      dw.out_m0 = 0;
+      dw_map = &mp.opt_part;
     }
-    g.add(mp.s_mn[b], mp.h_mn, mp.dw, dw);
+    g.add(mp.s_mn[b], mp.h_mn, *dw_map, dw);
     // dH[r0 : r0+rows, :] (=|+=) scale * staging * W[v0 : v0+cols, :]
     GemmParams dh = base_params(p, hdr);
     dh.m_tiles = (int)ceil_div(rows, kBM);
@@ -1029,7 +1095,7 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
       if (!launch_group(FLCE_KERNEL_GEMM_BWD, g, sms, st)) return FLCE_ERR_CUDA;
     } else {
       Group gw(gm), gh(gm), gz(gm);
-      gw.add(mp.s_mn[b], mp.h_mn, mp.dw, dw);
+      gw.add(mp.s_mn[b], mp.h_mn, *dw_map, dw);
       gh.add(mp.s_k[b], mp.w_mn, mp.dh, dh);
       if (!launch_group(FLCE_KERNEL_GEMM_DW, gw, sms, st)) return FLCE_ERR_CUDA;
       if (!launch_group(FLCE_KERNEL_GEMM_DH, gh, sms, st)) return FLCE_ERR_CUDA;
@@ -1037,6 +1103,17 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
         gz.add(mp.h_k, w_b, mp.s_store[b ^ 1], dz_next);
         if (!launch_group(FLCE_KERNEL_GEMM_DZ, gz, sms, st)) return FLCE_ERR_CUDA;
       }
+    }
+    if (vocab_major && rc == pl.row_chunks - 1) {
+      // The chunk's dW is complete: its AdamW step, before the next chunk's
+      // first contraction overwrites the buffer.
+      const float* part = reinterpret_cast<const float*>(ws + pl.off_opt_part);
+      const int64_t n4 = (int64_t)cols * p.hidden / 4;
+      const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * 8, ceil_div(n4, 256)));
+      ProfScope prof(FLCE_KERNEL_ADAMW_STEP, st);
+      adamw_rows_kernel<<<blocks, 256, 0, st>>>(hdr, part, cols, (int)p.hidden, vocab_map, v0, opt->master, opt->m,
+                                                 opt->v, opt->w_out);
+      if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
     }
     if (has_next && !count_skipped(dz_next, s + 1)) return FLCE_ERR_CUDA;
     if (has_next && !dbias_item(s + 1)) return FLCE_ERR_CUDA;
@@ -1069,6 +1146,9 @@ static bool build_maps(const flce_problem& p, const Plan& pl, const void* H, con
   }
   if (!make_map(&mp->dh, f32, dH, D, N, D * 4, 32, 32)) return false;
   if (dW && !make_map(&mp->dw, f32, dW, D, V, D * 4, 32, 32)) return false;
+  if (pl.off_opt_part &&
+      !make_map(&mp->opt_part, f32, ws + pl.off_opt_part, D, (uint64_t)pl.vc, D * 4, 32, 32))
+    return false;
   return true;
 }
 
@@ -1361,7 +1441,7 @@ flce_status flce_forward_backward_adamw(const flce_problem* p, const void* H, co
   if (!aligned(dH, 16) || !aligned(w_master, 16) || !aligned(adam_m, 16) || !aligned(adam_v, 16) ||
       !aligned(w_out, 16))
     return FLCE_ERR_UNSUPPORTED;
-  if (p->n_rows < 1 || p->n_rows > kRowChunk) return FLCE_ERR_UNSUPPORTED;
+  if (p->n_rows < 1) return FLCE_ERR_UNSUPPORTED;
   const size_t wbytes = (size_t)p->vocab * p->hidden * 2;
   if (overlaps(w_out, wbytes, W, wbytes)) return FLCE_ERR_INVALID_ARGUMENT;
   int sms = 0;

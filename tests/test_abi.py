@@ -40,11 +40,13 @@ def test_workspace_is_linear_in_rows_and_vocab_never_n_times_v():
     ws = flce.flce_workspace_bytes(p)
     logits = 8192 * 151552 * 2
     assert 0 < ws < logits / 5
-    # 16x the rows: O(N) growth only (row chunks reuse the same buffers).
+    # 16x the rows: O(N) growth (row chunks reuse the same buffers), plus one
+    # vocabulary chunk's fp32 dW for the fused optimizer once there are
+    # several row chunks.
     p_long = flce.make_problem(131072, 2048, 151552)
     ws_long = flce.flce_workspace_bytes(p_long)
-    assert ws_long - ws <= 131072 * 4 + (131072 // 256) * 8 + 4096
-    assert ws_long < 131072 * 151552 * 2 / 100
+    assert ws_long - ws <= 131072 * 4 + (131072 // 256) * 8 + 10240 * 2048 * 4 + 8192
+    assert ws_long < 131072 * 151552 * 2 / 50
     # Tiny problems need little.
     assert flce.flce_workspace_bytes(flce.make_problem(1, 8, 1)) < 1 << 20
 
@@ -109,8 +111,6 @@ def test_fused_adamw_argument_checks():
     assert call(w_out=W_ + wbytes - 16) == Status.ERR_INVALID_ARGUMENT     # overlaps W
     assert call(master=FAKE + 8) == Status.ERR_UNSUPPORTED                 # not 16-byte aligned
     assert call(n=nb - 1) == Status.ERR_WORKSPACE_TOO_SMALL
-    many = flce.make_problem(8193, 64, 100)
-    assert call(prob=many, n=flce.flce_workspace_bytes(many)) == Status.ERR_UNSUPPORTED
     none = flce.make_problem(0, 64, 100)
     assert call(prob=none, n=flce.flce_workspace_bytes(none)) == Status.ERR_UNSUPPORTED
 

@@ -272,3 +272,26 @@ def test_fused_step_with_filter_equals_filtered_gradient_then_step():
     assert flce.flce_adamw_step(hp, dW, *two, w_t, W.numel(), ws2.buf) == flce.Status.OK
     for a, b in zip(fused + [w_f, dH_f, loss_f], two + [w_t, dH_t, loss_t]):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("flags", [0, flce.FLAG_SORT_VOCAB])
+def test_fused_adamw_over_several_row_chunks(flags):
+    # 8492 rows: two row chunks, so each vocabulary chunk's dW is summed over
+    # both in the workspace before its AdamW step.
+    inp = small_inputs(8192 + 300, 64, 9000, seed=102, targets="zipf", ignore=0.1)
+    master, m, v = _state(inp, 12)
+    got = _gpu_step(inp, master, m, v, 5, flags)
+    _check(got, inp, master, m, v, 5)
+    # The same bits as the stored gradient followed by the standalone step.
+    H, W, y = to_device(inp)
+    dev = H.device
+    two = [torch.from_numpy(a.copy()).to(dev) for a in (master, m, v)]
+    w_t = torch.empty(W.shape, dtype=torch.bfloat16, device=dev)
+    hp = flce.adamw_hparams(HP["lr"], 5, (HP["beta1"], HP["beta2"]), HP["eps"], HP["weight_decay"], dev)
+    ws = flce.Workspace(dev)
+    loss, lse, dH, dW = flce.forward_backward(H, W, y, flags=flags, workspace=ws)
+    assert flce.flce_adamw_step(hp, dW, *two, w_t, W.numel(), ws.buf) == flce.Status.OK
+    assert np.array_equal(two[0].cpu().numpy(), got["master"])
+    assert np.array_equal(two[1].cpu().numpy(), got["m"]) and np.array_equal(two[2].cpu().numpy(), got["v"])
+    assert np.array_equal(w_t.view(torch.int16).cpu().numpy().view(np.uint16), got["w_out"])
+    assert np.array_equal(dH.cpu().numpy(), got["dH"])
