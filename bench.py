@@ -126,7 +126,7 @@ def recorded_traffic(workload: str):
 def gemm_kernel_name() -> str:
     """The GEMM variant the library launches (FLCE_GEMM_MODE, default pair)."""
     mode = os.environ.get("FLCE_GEMM_MODE", "pair")
-    return {"cta1": "flce_gemm_kernel<1>", "multicast": "flce_gemm_kernel<2>"}.get(mode, "flce_gemm_pair_kernel")
+    return "flce_gemm_kernel" if mode == "cta1" else "flce_gemm_pair_kernel"
 
 
 def measured_peaks():
@@ -217,6 +217,26 @@ def oracle_sample(inp, target_seconds: float):
             break
         rows = min(H64.shape[0], int(rows * max(2.0, min(8.0, target_seconds / 4 / max(dt, 1e-3)))))
     return rows / dt, rows, dt
+
+
+def host_cpu() -> dict:
+    """Architecture (uname -m) and CPU model of the host the oracle runs on."""
+    import platform
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model and os.path.exists("/proc/cpuinfo"):
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    return {"uname_m": platform.machine(), "cpu_model": model or "unknown"}
 
 
 def cpu_cores() -> int:
@@ -340,7 +360,11 @@ def run_ours(args, rank, world, local):
     traffic_gb, traffic_note = recorded_traffic(wl.name)
     gemm_ms = sum(v["ms"] for k, v in per_kind.items() if k.startswith("gemm_"))
     gemm_launches = sum(v["launches"] for k, v in per_kind.items() if k.startswith("gemm_"))
-    peak = float(peaks["bf16_tflops_sustained"])
+    # The timed region lasts well under the seconds-long back-to-back loop
+    # behind the sustained figure, so the kernel is held against the burst
+    # (dense bf16 cuBLAS, best of 10) peak; the sustained ratio is secondary.
+    peak = float(peaks["bf16_tflops"])
+    peak_sustained = float(peaks["bf16_tflops_sustained"])
     step_tflops = flops_step / (ms_per_step / 1e3) / 1e12
 
     skipped = flce.flce_get_filter_stats(ws, stream) if args.filter_eps > 0 else None
@@ -350,6 +374,7 @@ def run_ours(args, rank, world, local):
     flops_exec = flops_step if skipped is None else (4.0 + 4.0 * (1.0 - skipped)) * N * V * D
     achieved = flops_exec * args.steps / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
     fwd = run_forward_only(args, flce, torch, H, W, y, lse, loss, ws, prob, stream, N, D, V)
+    phases = phase_fractions(per_kind, args.steps, N, D, V, peak, skipped)
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -372,16 +397,20 @@ def run_ours(args, rank, world, local):
             "skipped_tile_fraction": skipped,
             "executed_tflop_per_step_at_least": (4.0 + 4.0 * (1.0 - skipped)) * N * V * D / 1e12},
         "pct_bf16_peak": 100.0 * step_tflops / peak,
-        "pct_bf16_peak_burst": 100.0 * step_tflops / float(peaks["bf16_tflops"]),
+        "pct_bf16_peak_sustained": 100.0 * step_tflops / peak_sustained,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": (achieved / peak) if achieved else None, "traffic": traffic_gb,
+                     "frac": (achieved / peak) if achieved else None,
+                     "frac_of_sustained": (achieved / peak_sustained) if achieved else None,
+                     "phases": phases, "traffic": traffic_gb,
                      "traffic_unit": "GB per launch (dram__bytes_read.sum + dram__bytes_write.sum)",
                      "traffic_source": traffic_note,
                      "kernel": gemm_kernel_name() + " (all four epilogues)",
                      "flops_per_launch": flops_exec / (gemm_launches / args.steps) if gemm_launches else None,
                      "flops_counted": "8NVD" if skipped is None else "executed, lower bound (filter on)",
                      "launches_per_step": gemm_launches / args.steps if gemm_launches else None,
-                     "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)"},
+                     "peak_kind": "burst",
+                     "peak_source": f"{peak_src} bf16_tflops (burst: the timed region lasts "
+                                    f"{total_ms_max / 1e3:.2f} s, shorter than the sustained loop)"},
         "kernel_ms_per_step": {k: v["ms"] / args.steps for k, v in sorted(per_kind.items())},
         # every launch of one untimed step, in order: (kind, device ms)
         "launches_one_step": one_step,
@@ -398,8 +427,25 @@ def run_ours(args, rank, world, local):
         v, rows, dt = oracle_sample(inp, args.cpu_seconds)
         result["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                                   "sample": f"first {rows} rows of the batch, full V and D, fp64 forward+backward, "
-                                            f"{dt:.1f} s"}
+                                            f"{dt:.1f} s", **host_cpu()}
     return result
+
+
+def phase_fractions(per_kind: dict, steps: int, n: int, d: int, v: int, peak: float, skipped) -> dict:
+    """Rate of the forward GEMM (2NVD over its launches) and of the backward
+    GEMMs (6NVD: recompute, dW and dH over theirs), per step and as a
+    fraction of `peak` TFLOP/s. With the filter on, the backward counts the
+    lower bound of the FLOPs it executed."""
+    def ms(*kinds):
+        return sum(per_kind[k]["ms"] for k in kinds if k in per_kind) / steps
+    fwd_ms = ms("gemm_lse")
+    bwd_ms = ms("gemm_dz", "gemm_bwd", "gemm_dw", "gemm_dh")
+    bwd_flops = (6.0 if skipped is None else 2.0 + 4.0 * (1.0 - skipped)) * n * v * d
+    out = {}
+    for name, flops, t in (("forward", 2.0 * n * v * d, fwd_ms), ("backward", bwd_flops, bwd_ms)):
+        tf = flops / (t / 1e3) / 1e12 if t > 0 else None
+        out[name] = {"ms_per_step": t, "tflops": tf, "frac": tf / peak if tf else None}
+    return out
 
 
 def run_forward_only(args, flce, torch, H, W, y, lse, loss, ws, prob, stream, N, D, V):
@@ -509,7 +555,8 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": wl.name, "n_rows": wl.n_rows, "hidden": wl.hidden, "vocab": wl.vocab},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle", "sample": sample,
+                             **host_cpu()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 

@@ -86,7 +86,8 @@ typedef struct {
 
 /* Test hook: every bounded wait inside the GEMM kernels gives up after about
  * a microsecond, so the timeout path runs and FLCE_ERR_TIMEOUT is recorded.
- * Outputs are then undefined. */
+ * Outputs are then undefined, except that a forward whose GEMM gave up
+ * writes NaN as its loss (mean and sum reductions). */
 #define FLCE_FLAG_TEST_SHORT_WAITS 0x1u
 
 /* With filter_eps > 0: apply the filter to one gradient only, as the
@@ -274,14 +275,17 @@ flce_status flce_get_vocab_order(const flce_problem* p, const void* ws, int32_t*
  *   Rows are processed in chunks small enough for the scratch. A problem
  *   whose buffers do not fit even with 256-row chunks (roughly V above two
  *   million) returns FLCE_ERR_UNSUPPORTED before launching anything.
- *   The first call on a device looks up the scratch's device address (a
- *   runtime API call); make that first call before any stream capture.
+ *   The first call on a device (and the first after its context was reset)
+ *   looks up the scratch's device address (a runtime API call); make that
+ *   first call before any stream capture.
  *   All calls share the one array and it keeps the last call's contents; the
  *   call initialises everything it reads. Calls that overlap on the GPU (on
  *   different streams, or from different threads) race on the scratch and
  *   must be serialised by the caller.
- *   Device-detected conditions (a bad target) are handled as in
- *   flce_forward, but are not reported: there is no workspace to query. */
+ *   There is no workspace to query for device-detected conditions. A bad
+ *   target is handled as in flce_forward (its row is ignored) and is not
+ *   reported. A bounded wait inside the kernels that ran out (an error of
+ *   the device, never expected) makes the loss NaN, as in every forward. */
 flce_status flce_forward_static_scratch(const flce_problem* p, const void* H, const void* W, const int64_t* y,
                                         float* lse, float* loss, void* stream);
 

@@ -170,9 +170,11 @@ __global__ void finalize_kernel(const double* __restrict__ block_sums, int n_blo
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    // reduction 0 = mean over the valid count (clamped to 1), 1 = sum, 2 = none
+    // reduction 0 = mean over the valid count (clamped to 1), 1 = sum, 2 = none.
+    // A forward whose GEMM gave up on a bounded wait has no valid partials:
+    // its loss is NaN, so no caller mistakes it for a result.
     const double denom = reduction == 0 ? (double)(hdr->count > 0 ? hdr->count : 1) : 1.0;
-    const float loss = (float)(red[0] / denom);
+    const float loss = (hdr->status & kDevTimeout) ? __int_as_float(0x7fc00000) : (float)(red[0] / denom);
     hdr->loss = loss;
     hdr->scale = reduction == 2 ? 1.0f : (float)((double)grad_loss / denom);
     if (reduction != 2) *loss_out = loss;
@@ -699,10 +701,7 @@ static bool device_setup(int* sms_out) {
   if (!info[dev].ready) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-    if (cudaFuncSetAttribute(flce_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kGemmSmemBytes) != cudaSuccess)
-      return false;
-    if (cudaFuncSetAttribute(flce_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(flce_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kGemmSmemBytes) != cudaSuccess)
       return false;
     const PairInstance* inst = pair_instances();
@@ -719,18 +718,15 @@ static bool device_setup(int* sms_out) {
 
 // Kernel variant of the GEMM launches:
 //   GEMM_CTA1       one CTA per tile, each loading its own A and B;
-//   GEMM_MULTICAST  2-CTA clusters on vertically adjacent tiles sharing the B
-//                   tile through TMA multicast;
 //   GEMM_PAIR       2-CTA clusters issuing tcgen05.mma.cta_group::2 (M = 256).
-// GEMM_PAIR is the default; FLCE_GEMM_MODE=cta1|multicast|pair overrides it.
-// With filtering, a 2-CTA variant leaves out a k-block only when both CTAs of
-// the group skip it (coarser dH mask: 256 rows instead of 128).
-enum GemmMode { GEMM_CTA1 = 1, GEMM_MULTICAST = 2, GEMM_PAIR = 3 };
+// GEMM_PAIR is the default; FLCE_GEMM_MODE=cta1|pair overrides it.
+// With filtering, the pair leaves out a k-block only when both of its CTAs
+// skip it (coarser dH mask: 256 rows instead of 128).
+enum GemmMode { GEMM_CTA1 = 1, GEMM_PAIR = 3 };
 
 static GemmMode gemm_mode() {
   static GemmMode mode = [] {
     const char* e = std::getenv("FLCE_GEMM_MODE");
-    if (e && std::strcmp(e, "multicast") == 0) return GEMM_MULTICAST;
     if (e && std::strcmp(e, "cta1") == 0) return GEMM_CTA1;
     return GEMM_PAIR;
   }();
@@ -808,7 +804,7 @@ static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
   ProfScope prof(kind, st);
   if (g.mode == GEMM_CTA1) {
     const int grid = std::min(g.units, sms);
-    flce_gemm_kernel<1><<<grid, kGemmThreads, kGemmSmemBytes, st>>>(g.L);
+    flce_gemm_kernel<<<grid, kGemmThreads, kGemmSmemBytes, st>>>(g.L);
     return cudaGetLastError() == cudaSuccess;
   }
   const int grid = 2 * std::min(g.units, sms / 2);
@@ -816,7 +812,6 @@ static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = kGemmSmemBytes;   // the pair instances set their own below
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -825,24 +820,21 @@ static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (g.mode == GEMM_PAIR) {
-    bool skip = false;
-    int modes = 0;
-    for (int q = 0; q < g.L.n_probs; ++q) {
-      skip = skip || g.L.prob[q].skip_by_flags != 0;
-      modes |= 1 << g.L.prob[q].mode;
-    }
-    const PairInstance* inst = pair_instances();
-    for (int i = 0; i < kPairInstances; ++i) {
-      if (inst[i].skip != skip || (modes & ~inst[i].modes) != 0) continue;
-      cfg.dynamicSmemBytes = inst[i].smem;
-      GemmLaunch L = g.L;
-      L.order_groups = (modes & kModeAdamw) ? adamw_order_groups() : 1;
-      return cudaLaunchKernelEx(&cfg, inst[i].fn, L) == cudaSuccess;
-    }
-    return false;   // no instance carries this set of epilogues
+  bool skip = false;
+  int modes = 0;
+  for (int q = 0; q < g.L.n_probs; ++q) {
+    skip = skip || g.L.prob[q].skip_by_flags != 0;
+    modes |= 1 << g.L.prob[q].mode;
   }
-  return cudaLaunchKernelEx(&cfg, flce_gemm_kernel<2>, g.L) == cudaSuccess;
+  const PairInstance* inst = pair_instances();
+  for (int i = 0; i < kPairInstances; ++i) {
+    if (inst[i].skip != skip || (modes & ~inst[i].modes) != 0) continue;
+    cfg.dynamicSmemBytes = inst[i].smem;
+    GemmLaunch L = g.L;
+    L.order_groups = (modes & kModeAdamw) ? adamw_order_groups() : 1;
+    return cudaLaunchKernelEx(&cfg, inst[i].fn, L) == cudaSuccess;
+  }
+  return false;   // no instance carries this set of epilogues
 }
 
 struct Maps {
@@ -1322,20 +1314,41 @@ static flce_status check_common(const flce_problem* p, const void* H, const void
 // that every GPU loading this library holds until the process exits. Host
 // code must not pass the symbol itself to a kernel (on the host it names a
 // stand-in object, not device memory); the device address comes from
-// cudaGetSymbolAddress, looked up once per device.
+// cudaGetSymbolAddress, looked up once per device and context: a context
+// torn down and created again (cudaDeviceReset) loads the module afresh, and
+// the array may then sit at another address.
 constexpr size_t kStaticScratchBytes = (size_t)16 << 20;
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
+static PFN_cuCtxGetCurrent_v4000 ctx_current_fn() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  });
+  return fn;
+}
+
+// Called after device_setup, so the device's primary context is current.
 static bool static_scratch_address(void** out) {
   static std::mutex mu;
   static void* addr[64] = {};
+  static CUcontext ctx_of[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  CUcontext ctx = nullptr;
+  PFN_cuCtxGetCurrent_v4000 get_ctx = ctx_current_fn();
+  if (!get_ctx || get_ctx(&ctx) != CUDA_SUCCESS || !ctx) return false;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!addr[dev] || ctx_of[dev] != ctx) {
     void* a = nullptr;
     if (cudaGetSymbolAddress(&a, g_static_scratch) != cudaSuccess || !a) return false;
     addr[dev] = a;
+    ctx_of[dev] = ctx;
   }
   *out = addr[dev];
   return true;

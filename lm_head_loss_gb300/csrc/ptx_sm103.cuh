@@ -245,18 +245,6 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// TMA tiled load whose data and complete_tx land at the same shared-memory
-// offset in every CTA of the cluster named in cta_mask.
-__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUtensorMap* m, int32_t c0, int32_t c1,
-                                                      uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;"
-      ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar)),
-        "h"(cta_mask)
-      : "memory");
-}
-
 // Arrive on an mbarrier given by its shared::cluster address (possibly in a
 // peer CTA of the cluster).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
@@ -268,15 +256,6 @@ __device__ __forceinline__ uint32_t map_to_rank(const void* p, uint32_t rank) {
   uint32_t out;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(p)), "r"(rank));
   return out;
-}
-
-// Arrive once, when this thread's tcgen05 operations so far have completed,
-// on the mbarrier at the same offset in every CTA named in cta_mask.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-      ::"r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
 }
 
 }  // namespace ptx

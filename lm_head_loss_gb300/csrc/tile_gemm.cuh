@@ -155,8 +155,9 @@ static_assert(sizeof(GemmParams) % 128 == 0 && offsetof(GemmLaunch, prob) % 128 
               "problem parameters on 128-byte boundaries");
 static_assert(sizeof(GemmLaunch) <= 4096, "kernel parameter block");
 
-// Tiles are counted in groups of kCluster vertically adjacent m-tiles that
-// share one n-tile (one group per cluster); with kCluster = 1 a group is a tile.
+// Tiles are counted in groups of `cluster` vertically adjacent m-tiles that
+// share one n-tile (an SM pair of the pair kernel); with cluster = 1 a group
+// is a tile.
 __device__ __forceinline__ int m_groups(const GemmParams& p, int cluster) { return (p.m_tiles + cluster - 1) / cluster; }
 
 __device__ __forceinline__ int decode_tile(const GemmLaunch& L, int t, int& pi) {
@@ -551,12 +552,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
   }
 }
 
-// kCluster = 1: every CTA loads its own A and B tiles.
-// kCluster = 2: the two CTAs of a cluster take vertically adjacent m-tiles of
-// the same n-tile; each loads its own A tile and one half of the shared B tile
-// and multicasts that half into both CTAs, so the cluster reads B from L2 once.
-// A shared-memory stage is refilled only after both CTAs' MMAs have read it.
-template <int kCluster>
+// One CTA per 128x256 tile: every CTA loads its own A and B tiles into a
+// 4-stage ring and issues tcgen05.mma.cta_group::1 (M = 128). The pair
+// kernel (tile_gemm_pair.cuh) is the default; this one is kept for
+// comparison (FLCE_GEMM_MODE=cta1).
 __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid_constant__ GemmLaunch L) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
@@ -574,17 +573,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int num_tiles = L.tile_end[L.n_probs - 1];
-  const int rank = kCluster > 1 ? (int)ptx::cluster_ctarank() : 0;
-  const int unit0 = blockIdx.x / kCluster;
-  const int unit_stride = gridDim.x / kCluster;
-  constexpr uint16_t kPeers = (uint16_t)((1u << kCluster) - 1u);
+  const int unit0 = blockIdx.x;
+  const int unit_stride = gridDim.x;
   const uint64_t wait_limit_ns = L.prob[0].wait_limit_ns;
   uint32_t* const status = L.prob[0].status;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
-      ptx::mbar_init(&empty_bar[s], kCluster);
+      ptx::mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&acc_full[b], 1);
@@ -605,7 +602,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (kCluster > 1) ptx::cluster_sync_all();   // peers' barriers exist before any multicast
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -622,10 +618,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
         const GemmParams& p = L.prob[pi];
         const CUtensorMap* tmA = &L.tm_a[pi];
         const CUtensorMap* tmB = &L.tm_b[pi];
-        tile_coords(p, tl, kCluster, rank, mt, nt);
-        const int mt_first = mt - rank;
+        tile_coords(p, tl, 1, 0, mt, nt);
         const bool may_skip = p.skip_by_flags != 0;
-        const uint64_t keep = may_skip ? tile_keep(p, mt_first, kCluster) : ~0ull;
+        const uint64_t keep = may_skip ? tile_keep(p, mt, 1) : ~0ull;
         const int k_blocks = p.k_blocks;
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (may_skip && kblock_dropped(p, keep, kb)) continue;
@@ -644,24 +639,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
           } else {
             ptx::tma_load_2d(sa, tmA, p.a_k0 + kc, p.a_m0 + mt * kBM, &full_bar[stage]);
           }
-          if (kCluster == 1) {
-            if (p.b_mn) {
-              for (int h = 0; h < kBN / 64; ++h)
-                ptx::tma_load_2d(sb + h * 8192, tmB, p.b_n0 + nt * kBN + h * 64, p.b_k0 + kc, &full_bar[stage]);
-            } else {
-              ptx::tma_load_2d(sb, tmB, p.b_k0 + kc, p.b_n0 + nt * kBN, &full_bar[stage]);
-            }
+          if (p.b_mn) {
+            for (int h = 0; h < kBN / 64; ++h)
+              ptx::tma_load_2d(sb + h * 8192, tmB, p.b_n0 + nt * kBN + h * 64, p.b_k0 + kc, &full_bar[stage]);
           } else {
-            // This CTA's share of the B tile: rows [rank * kBN / kCluster, ...).
-            constexpr int kShare = kBN / kCluster;
-            if (p.b_mn) {
-              for (int h = rank * (kShare / 64); h < (rank + 1) * (kShare / 64); ++h)
-                ptx::tma_load_2d_multicast(sb + h * 8192, tmB, p.b_n0 + nt * kBN + h * 64, p.b_k0 + kc,
-                                           &full_bar[stage], kPeers);
-            } else {
-              ptx::tma_load_2d_multicast(sb + rank * kShare * 128, tmB, p.b_k0 + kc, p.b_n0 + nt * kBN + rank * kShare,
-                                         &full_bar[stage], kPeers);
-            }
+            ptx::tma_load_2d(sb, tmB, p.b_k0 + kc, p.b_n0 + nt * kBN, &full_bar[stage]);
           }
           last_parity[stage] = (int32_t)phase;
           if (++stage == kStages) {
@@ -689,8 +671,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
         int pi, mt, nt;
         const int tl = decode_tile(L, t, pi);
         const GemmParams& p = L.prob[pi];
-        tile_coords(p, tl, kCluster, rank, mt, nt);
-        const int mt_first = mt - rank;
+        tile_coords(p, tl, 1, 0, mt, nt);
         const uint32_t idesc = ptx::idesc_bf16_f32(kBM, kBN, p.a_mn != 0, p.b_mn != 0);
         const uint32_t buf = i & 1, use = i >> 1;
         if (!ptx::mbar_wait_bounded(&acc_empty[buf], (use & 1u) ^ 1u, wait_limit_ns, abort_flag)) {
@@ -702,8 +683,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
         const uint32_t d_tmem = tmem_base + buf * kBN;
         uint32_t accumulate = 0;
         const bool may_skip = p.skip_by_flags != 0;
-        const uint64_t keep = may_skip ? tile_keep(p, mt_first, kCluster) : ~0ull;
-        const uint64_t own_keep = may_skip ? tile_keep(p, mt, 1) : ~0ull;
+        const uint64_t keep = may_skip ? tile_keep(p, mt, 1) : ~0ull;
         const int k_blocks = p.k_blocks;
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (may_skip && kblock_dropped(p, keep, kb)) continue;
@@ -713,26 +693,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
             break;
           }
           ptx::tc_fence_after();
-          // In a cluster, a stage the group loads for the peer may still be
-          // one this CTA's own tile skips: it then issues no MMA but still
-          // releases the stage.
-          if (kCluster == 1 || !may_skip || !kblock_dropped(p, own_keep, kb)) {
-            const uint32_t a_addr = smem_base + stage * kStageBytes;
-            const uint32_t b_addr = a_addr + kABytes;
+          const uint32_t a_addr = smem_base + stage * kStageBytes;
+          const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              const uint64_t adesc = p.a_mn ? ptx::smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
-                                            : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
-              const uint64_t bdesc = p.b_mn ? ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
-                                            : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
-              ptx::mma_bf16_ss(d_tmem, adesc, bdesc, idesc, accumulate);
-              accumulate = 1;
-            }
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t adesc = p.a_mn ? ptx::smem_desc_sw128(a_addr + k * 2048, 8192, 1024)
+                                          : ptx::smem_desc_sw128(a_addr + k * 32, 16, 1024);
+            const uint64_t bdesc = p.b_mn ? ptx::smem_desc_sw128(b_addr + k * 2048, 8192, 1024)
+                                          : ptx::smem_desc_sw128(b_addr + k * 32, 16, 1024);
+            ptx::mma_bf16_ss(d_tmem, adesc, bdesc, idesc, accumulate);
+            accumulate = 1;
           }
-          if (kCluster == 1)
-            ptx::mma_commit(&empty_bar[stage]);
-          else
-            ptx::mma_commit_multicast(&empty_bar[stage], kPeers);
+          ptx::mma_commit(&empty_bar[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -758,7 +730,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
       const int tl = decode_tile(L, t, pi);
       const GemmParams& p = L.prob[pi];
       const CUtensorMap* tmOut = &L.tm_out[pi];
-      tile_coords(p, tl, kCluster, rank, mt, nt);
+      tile_coords(p, tl, 1, 0, mt, nt);
       const uint32_t buf = i & 1, use = i >> 1;
       if (!ptx::mbar_wait_bounded(&acc_full[buf], use & 1u, wait_limit_ns, abort_flag)) {
         record_timeout(status, abort_flag);
@@ -776,7 +748,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (kCluster > 1) ptx::cluster_sync_all();   // no peer still multicasts into this CTA
   ptx::tc_fence_after();
   if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
 }

@@ -90,5 +90,5 @@ def assert_parity(got, ref, loss_rel=LOSS_REL, lse_abs=LSE_ABS, grad_rel=GRAD_RE
 def dh_filter_rows() -> int:
     """Height of the dH tile mask of the GEMM variant in use: the default pair
     kernel leaves a dH k-block out only when both of its 128-row halves are
-    filtered; the 1-CTA and multicast variants filter 128-row tiles."""
-    return 128 if os.environ.get("FLCE_GEMM_MODE") in ("cta1", "multicast") else 256
+    filtered; the 1-CTA variant filters 128-row tiles."""
+    return 128 if os.environ.get("FLCE_GEMM_MODE") == "cta1" else 256

@@ -485,3 +485,60 @@ def test_fused_step_equals_gradient_then_optimizer():
     opt.step()
     assert np.max(np.abs(r["master"] - tp.detach().numpy())) < 1e-14
     assert r["count"] == count and abs(r["loss"] - loss) < 1e-15
+
+
+# ---------------------------------------------------------------- input widening
+# Every parity test feeds both sides the same bf16 inputs and the oracle widens
+# them to fp64 (inputs_f64). These pins check that widening against two
+# decoders that share nothing with it: torch's own bfloat16 -> float64
+# conversion, and the bf16 format written out with integers (1 sign bit,
+# 8 exponent bits with bias 127, 7 fraction bits; subnormals at exponent 0).
+
+def _decode_bf16_by_fields(bits: int) -> float:
+    sign = -1.0 if bits & 0x8000 else 1.0
+    exp = (bits >> 7) & 0xFF
+    frac = bits & 0x7F
+    if exp == 0xFF:
+        assert frac == 0, "NaN patterns are not decoded here"
+        return sign * math.inf
+    if exp == 0:
+        return sign * math.ldexp(frac / 128.0, -126)
+    return sign * math.ldexp(1.0 + frac / 128.0, exp - 127)
+
+
+def _all_non_nan_bf16_patterns() -> np.ndarray:
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    exp = (bits >> 7) & 0xFF
+    frac = bits & 0x7F
+    return bits[~((exp == 0xFF) & (frac != 0))].astype(np.uint16)
+
+
+def test_inputs_f64_matches_torch_on_every_bf16_pattern():
+    bits = _all_non_nan_bf16_patterns()
+    assert bits.size == (1 << 16) - 2 * 127     # NaNs excluded, both infinities kept
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    h64, w64 = oracle.inputs_f64(bits.reshape(2, -1), bits[::-1].reshape(-1, 2))
+    assert h64.dtype == np.float64 and w64.dtype == np.float64
+    assert h64.shape == (2, bits.size // 2) and w64.shape == (bits.size // 2, 2)
+    np.testing.assert_array_equal(h64.ravel(), ref)
+    np.testing.assert_array_equal(w64.ravel(), ref[::-1])     # the second array is W's, not H's again
+    assert np.array_equal(np.signbit(h64.ravel()), np.signbit(ref))   # -0 stays -0
+
+
+def test_inputs_f64_matches_the_bit_fields_on_every_bf16_pattern():
+    bits = _all_non_nan_bf16_patterns()
+    ref = np.array([_decode_bf16_by_fields(int(b)) for b in bits], dtype=np.float64)
+    got, _ = oracle.inputs_f64(bits, bits[:1])
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("bits,value", [
+    (0x3F80, 1.0), (0xBF80, -1.0), (0x4000, 2.0), (0x3F00, 0.5), (0x3FC0, 1.5),
+    (0x0001, 2.0 ** -133),                     # smallest subnormal
+    (0x0080, 2.0 ** -126),                     # smallest normal
+    (0x7F7F, (2.0 - 2.0 ** -7) * 2.0 ** 127),  # largest finite
+    (0x7F80, math.inf), (0xFF80, -math.inf), (0x8000, -0.0), (0x0000, 0.0),
+])
+def test_inputs_f64_known_values(bits, value):
+    got, _ = oracle.inputs_f64(np.array([bits], dtype=np.uint16), np.zeros(1, dtype=np.uint16))
+    assert got[0] == value and math.copysign(1.0, got[0]) == math.copysign(1.0, value)

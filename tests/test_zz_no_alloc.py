@@ -59,3 +59,29 @@ def test_static_scratch_rejects_problems_beyond_its_size():
     loss = torch.empty((), device="cuda")
     too_big = flce.make_problem(16, 8, 4_000_000)   # never launched: rejected on the host
     assert flce.flce_forward_static_scratch(too_big, H, W, y, lse, loss) == flce.Status.ERR_UNSUPPORTED
+
+
+def test_static_scratch_matches_the_oracle():
+    import oracle
+    inp = small_inputs(700, 128, 9000, seed=5, targets="zipf", ignore=0.05)
+    H, W, y = to_device(inp)
+    loss, lse = _static(flce.make_problem(700, 128, 9000), H, W, y)
+    H64, W64 = oracle.inputs_f64(inp["H"], inp["W"])
+    r_lse, r_loss, _ = oracle.forward(H64, W64, inp["y"])
+    assert abs(loss - r_loss) <= LOSS_REL * abs(r_loss)
+    assert np.max(np.abs(lse - r_lse)) <= LSE_ABS
+
+
+def test_static_scratch_reports_a_timed_out_forward_as_nan_loss():
+    # With every bounded wait cut to about a microsecond the forward GEMM
+    # gives up; with no workspace to query, the NaN loss is the report. The
+    # next call starts from a clean scratch and matches flce_forward.
+    inp = small_inputs(512, 256, 4096, seed=11)
+    H, W, y = to_device(inp)
+    loss, _ = _static(flce.make_problem(512, 256, 4096, flags=flce.FLAG_TEST_SHORT_WAITS), H, W, y)
+    assert np.isnan(loss)
+    prob = flce.make_problem(512, 256, 4096)
+    ref_loss, ref_lse = _with_workspace(prob, H, W, y)
+    loss, lse = _static(prob, H, W, y)
+    assert abs(loss - ref_loss) <= LOSS_REL * abs(ref_loss)
+    assert np.max(np.abs(lse - ref_lse)) <= LSE_ABS
