@@ -7,9 +7,11 @@ V = 151,552, bf16 inputs, fp32 outputs), with the inputs resident in HBM.
 W alone (592 MiB) is larger than the 129 MB L2, so no L2 flush is added
 between steps.
 
-Prints one JSON line (rank 0). Under torchrun every rank runs its own batch
-on its own GPU with no collective in the data path (weak scaling); the step
-time is the maximum over ranks.
+Prints one JSON line (rank 0). Under torchrun every rank holds its own batch
+of N rows and the whole W, and a step is the data-parallel one
+(DataParallelStep): the valid count is summed over the ranks before the
+forward and backward, the loss and dW after them (NCCL), all inside the
+timed region (weak scaling); the step time is the maximum over ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -265,17 +267,31 @@ def run_ours(args, rank, world, local):
         flce.FLAG_SORT_VOCAB if args.sort_vocab else 0)
     prob = flce.make_problem(N, D, V, -100, args.filter_eps, flags)
     ws_bytes = flce.flce_workspace_bytes(prob)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    loss = torch.empty((), dtype=torch.float32, device=dev)
-    lse = torch.empty(N, dtype=torch.float32, device=dev)
-    dH = torch.empty(N, D, dtype=torch.float32, device=dev)
-    dW = torch.empty(V, D, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    if world > 1:
+        # Data parallel over rows: this rank's batch, the whole W; the valid
+        # count, the loss and dW are summed over the ranks (NCCL) every step.
+        if args.adamw != "none":
+            raise SystemExit("--adamw takes one GPU: the fused update needs the complete dW of every rank")
+        dp = flce.DataParallelStep(N, D, V, dev, filter_eps=args.filter_eps, flags=flags)
+        ws, loss, lse, dH, dW = dp.ws, dp.loss, dp.lse, dp.dH, dp.dW
+
+        def fwd_bwd(H_, W_, y_):
+            dp(H_, W_, y_)
+    else:
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        loss = torch.empty((), dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+        dH = torch.empty(N, D, dtype=torch.float32, device=dev)
+        dW = torch.empty(V, D, dtype=torch.float32, device=dev)
+
+        def fwd_bwd(H_, W_, y_):
+            st = flce.flce_forward_backward(prob, H_, W_, y_, 1.0, lse, loss, dH, dW, ws, stream=stream)
+            if st != flce.Status.OK:
+                raise flce.FlceError(st, "flce_forward_backward")
 
     def step():
-        st = flce.flce_forward_backward(prob, H, W, y, 1.0, lse, loss, dH, dW, ws, stream=stream)
-        if st != flce.Status.OK:
-            raise flce.FlceError(st, "flce_forward_backward")
+        fwd_bwd(H, W, y)
 
     if args.adamw != "none":
         # Optimizer state of W: fp32 master and moments, a second bf16 copy.
@@ -383,7 +399,8 @@ def run_ours(args, rank, world, local):
                    "targets": wl.targets, "ignore_frac": wl.ignore_frac, "filter_eps": args.filter_eps,
                    "compact_ignored": bool(args.compact_ignored), "sort_vocab": bool(args.sort_vocab),
                    "adamw_on_W": args.adamw,
-                   "parallelism": f"dp{world} (independent batches, no collective)",
+                   "parallelism": (f"dp{world}: rows sharded, W replicated; valid count, loss and dW "
+                                   f"all-reduced over NCCL inside the timed region") if world > 1 else "dp1",
                    "l2": "no flush: W (592 MiB bf16) alone exceeds the 129 MB L2 every step"},
         "tflops": step_tflops,
         "step_ms_median": statistics.median(step_ms),
@@ -422,7 +439,7 @@ def run_ours(args, rank, world, local):
     }
 
     if not args.no_e2e and args.adamw == "none":
-        result["e2e"] = run_e2e(args, flce, torch, inp, prob, ws, (loss, lse, dH, dW), dev, stream, world, dist)
+        result["e2e"] = run_e2e(args, torch, inp, fwd_bwd, loss, dev, stream, world, dist)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, rows, dt = oracle_sample(inp, args.cpu_seconds)
         result["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
@@ -464,12 +481,11 @@ def run_forward_only(args, flce, torch, H, W, y, lse, loss, ws, prob, stream, N,
     return {"ms_per_step": ms, "tokens_per_s": N / (ms / 1e3), "tflops": 2.0 * N * V * D / (ms / 1e3) / 1e12}
 
 
-def run_e2e(args, flce, torch, inp, prob, ws, outs, dev, stream, world, dist):
+def run_e2e(args, torch, inp, fwd_bwd, loss, dev, stream, world, dist):
     """Same step through the public API from pinned HOST buffers: every step
     copies that step's H, W and y to the device and reads its loss back.
     As in a real input pipeline, the copy of step i+1 runs on a second
     stream into a second set of device buffers while step i computes."""
-    loss, lse, dH, dW = outs
     hH = torch.from_numpy(inp["H"].view(np.int16)).view(torch.bfloat16).pin_memory()
     hW = torch.from_numpy(inp["W"].view(np.int16)).view(torch.bfloat16).pin_memory()
     hy = torch.from_numpy(inp["y"]).pin_memory()
@@ -496,11 +512,9 @@ def run_e2e(args, flce, torch, inp, prob, ws, outs, dev, stream, world, dist):
         b = i % 2
         stream.wait_event(copied[b])
         H, W, y = bufs[b]
-        st = flce.flce_forward_backward(prob, H, W, y, 1.0, lse, loss, dH, dW, ws, stream=stream)
-        if st != flce.Status.OK:
-            raise flce.FlceError(st, "flce_forward_backward")
+        fwd_bwd(H, W, y)
         consumed[b].record(stream)
-        hloss[i].copy_(loss, non_blocking=True)
+        hloss[i].copy_(loss.view(()), non_blocking=True)
 
     def run(n):
         copy_in(0)

@@ -155,6 +155,38 @@ flce_status flce_forward_backward(const flce_problem* p, const void* H, const vo
                                   float grad_loss, float* lse, float* loss, float* dH, float* dW, void* ws,
                                   size_t ws_bytes, void* stream);
 
+/* Data parallelism over rows: each process (one per GPU) holds its own rows
+ * H, y and the whole W, and the ranks together take the mean over the valid
+ * rows of ALL ranks. The pages name the exchange this needs: data
+ * parallelism all-reduces the weight gradient (the FORGE explainer, on what
+ * its fused update cannot cover), and the PyTorch 2.13 chapter lists
+ * sharding the LM head across devices among its open items. One step:
+ *   1. flce_count_valid on every rank, then a sum of the counts over the
+ *      ranks (the caller's all-reduce, e.g. NCCL on the same stream);
+ *   2. flce_forward_backward_global with that sum;
+ *   3. a sum over the ranks of the loss and of dW (the caller's
+ *      all-reduce); dH and lse stay per rank, since each rank owns its rows.
+ *
+ * flce_count_valid: *count (device int64) = the number of this rank's targets
+ * in [0, V) that are not ignore_index (the rows a mean counts; bad targets
+ * are not counted). Enqueued on `stream`; y and count 8-byte aligned.
+ * FLCE_ERR_INVALID_ARGUMENT on a bad problem or pointer. */
+flce_status flce_count_valid(const flce_problem* p, const int64_t* y, int64_t* count, void* stream);
+
+/* flce_forward_backward with the mean taken over *count_global (device
+ * int64, read on `stream` after the caller's all-reduce; the sum of every
+ * rank's flce_count_valid) instead of this call's own count:
+ *   loss = sum over this rank's valid rows of (LSE_n - z_{n,y_n}) / max(count_global, 1),
+ *          this rank's share of the global mean (the shares sum to it);
+ *   dH, dW = grad_loss / max(count_global, 1) * (the same sums as
+ *          flce_forward_backward), so dW is this rank's contribution and the
+ *          sum of dW over the ranks is the gradient of the global mean.
+ * Every other argument, output and error is as in flce_forward_backward;
+ * count_global must be 8-byte aligned. */
+flce_status flce_forward_backward_global(const flce_problem* p, const void* H, const void* W, const int64_t* y,
+                                         const int64_t* count_global, float grad_loss, float* lse, float* loss,
+                                         float* dH, float* dW, void* ws, size_t ws_bytes, void* stream);
+
 /* Reductions of the per-row losses for the general entry points below. */
 #define FLCE_REDUCTION_MEAN 0 /* sum over valid rows / max(count, 1) */
 #define FLCE_REDUCTION_SUM 1  /* sum over valid rows */
@@ -314,6 +346,7 @@ flce_status flce_forward_static_scratch(const flce_problem* p, const void* H, co
 #define FLCE_KERNEL_VOCAB_GATHER 13 /* W, bias and targets rearranged in the sorted order */
 #define FLCE_KERNEL_ADAMW_PREP 14   /* constants of an AdamW step */
 #define FLCE_KERNEL_ADAMW_STEP 15   /* flce_adamw_step's elementwise update */
+#define FLCE_KERNEL_COUNT 16        /* flce_count_valid */
 flce_status flce_profile_set(void** events, int32_t* kinds, int32_t cap);
 int32_t flce_profile_count(void);
 

@@ -22,7 +22,9 @@ from ._binding import (  # noqa: F401
     flce_forward,
     flce_adamw_step,
     flce_backward_ex,
+    flce_count_valid,
     flce_forward_backward,
+    flce_forward_backward_global,
     flce_forward_backward_adamw,
     flce_forward_ex,
     flce_forward_static_scratch,
@@ -38,3 +40,4 @@ from ._binding import (  # noqa: F401
 from .api import (FusedAdamWHead, Workspace, adamw_hparams, device_status, forward,  # noqa: F401
                   forward_backward, forward_backward_adamw)
 from .autograd import FusedLinearCrossEntropy, linear_cross_entropy  # noqa: F401
+from .data_parallel import DataParallelStep, exchange_step  # noqa: F401

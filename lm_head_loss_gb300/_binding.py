@@ -90,6 +90,10 @@ def _load() -> ctypes.CDLL:
     lib.flce_forward.restype = ctypes.c_int
     lib.flce_forward_backward.argtypes = [prob, vp, vp, vp, f32, vp, vp, vp, vp, vp, sz, vp]
     lib.flce_forward_backward.restype = ctypes.c_int
+    lib.flce_count_valid.argtypes = [prob, vp, vp, vp]
+    lib.flce_count_valid.restype = ctypes.c_int
+    lib.flce_forward_backward_global.argtypes = [prob, vp, vp, vp, vp, f32, vp, vp, vp, vp, vp, sz, vp]
+    lib.flce_forward_backward_global.restype = ctypes.c_int
     lib.flce_forward_backward_adamw.argtypes = [prob, vp, vp, vp, f32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.flce_forward_backward_adamw.restype = ctypes.c_int
     lib.flce_adamw_step.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, vp]
@@ -168,6 +172,23 @@ def flce_forward_backward(problem, H, W, y, grad_loss: float, lse, loss, dH, dW,
                                             _addr(dH), _addr(dW), _addr(ws), nb, _stream(stream)))
 
 
+def flce_count_valid(problem, y, count, stream=None) -> Status:
+    """Number of valid targets of these rows into `count` (device int64 [1])."""
+    return Status(lib.flce_count_valid(ctypes.byref(problem) if problem is not None else None, _addr(y),
+                                       _addr(count), _stream(stream)))
+
+
+def flce_forward_backward_global(problem, H, W, y, count_global, grad_loss: float, lse, loss, dH, dW, ws,
+                                 ws_bytes: int | None = None, stream=None) -> Status:
+    """flce_forward_backward with the mean over `count_global` (device int64
+    [1], the valid count of every rank of a data-parallel step)."""
+    nb = _nbytes(ws) if ws_bytes is None else ws_bytes
+    return Status(lib.flce_forward_backward_global(ctypes.byref(problem) if problem is not None else None, _addr(H),
+                                                   _addr(W), _addr(y), _addr(count_global), float(grad_loss),
+                                                   _addr(lse), _addr(loss), _addr(dH), _addr(dW), _addr(ws), nb,
+                                                   _stream(stream)))
+
+
 def flce_forward_backward_adamw(problem, H, W, y, grad_loss: float, lse, loss, dH, w_master, adam_m, adam_v, w_out,
                                 hparams, ws, ws_bytes: int | None = None, stream=None) -> Status:
     nb = _nbytes(ws) if ws_bytes is None else ws_bytes
@@ -232,7 +253,7 @@ def flce_get_vocab_order(problem, ws, order, avg_logit=None, stream=None) -> Sta
 KERNEL_KINDS = {0: "gemm_lse", 1: "gemm_dz", 2: "gemm_dw", 3: "gemm_dh", 4: "prep", 5: "combine",
                 6: "finalize", 7: "filter_stats", 8: "gemm_bwd", 9: "dbias", 10: "set_scale",
                 11: "vocab_keys", 12: "vocab_sort", 13: "vocab_gather", 14: "adamw_prep",
-                15: "adamw_step"}
+                15: "adamw_step", 16: "count"}
 
 
 class LaunchProfiler:

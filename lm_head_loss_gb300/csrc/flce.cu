@@ -102,6 +102,26 @@ __global__ void prep_kernel(const int64_t* __restrict__ y, int64_t n, int64_t vo
   }
 }
 
+// One block: the number of targets in [0, V) that are not ignore_index
+// (the rows a mean counts), written to *count.
+__global__ void count_valid_kernel(const int64_t* __restrict__ y, int64_t n, int64_t vocab, int64_t ignore_index,
+                                   int64_t* __restrict__ count) {
+  __shared__ long long s_cnt[32];
+  long long cnt = 0;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const int64_t t = y[i];
+    cnt += (t != ignore_index && t >= 0 && t < vocab) ? 1 : 0;
+  }
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_down_sync(0xffffffffu, cnt, o);
+  if ((threadIdx.x & 31) == 0) s_cnt[threadIdx.x >> 5] = cnt;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long c = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) c += s_cnt[i];
+    *count = c;
+  }
+}
+
 // Merge of the per-tile (max, sum) partials into LSE_n. A block covers 32
 // rows; thread (r, g) merges tiles g, g + 8, g + 16, ... of row r, then the 8
 // partials of a row are merged in g order and the 32 row losses of the block
@@ -158,8 +178,10 @@ __global__ void __launch_bounds__(kCombineRows * kCombineSplit)
 
 // One block: fixed-order fp64 sum of the per-block row losses, mean over the
 // valid count (clamped to one), and the gradient scale g / count.
+// count_global (or NULL): the valid count of every rank of a data-parallel
+// step, which replaces this call's own count in the mean.
 __global__ void finalize_kernel(const double* __restrict__ block_sums, int n_blocks, float grad_loss, WsHeader* hdr,
-                                float* loss_out, int reduction) {
+                                float* loss_out, int reduction, const int64_t* __restrict__ count_global) {
   __shared__ double red[256];
   double acc = 0.0;
   for (int i = threadIdx.x; i < n_blocks; i += 256) acc += block_sums[i];
@@ -173,7 +195,8 @@ __global__ void finalize_kernel(const double* __restrict__ block_sums, int n_blo
     // reduction 0 = mean over the valid count (clamped to 1), 1 = sum, 2 = none.
     // A forward whose GEMM gave up on a bounded wait has no valid partials:
     // its loss is NaN, so no caller mistakes it for a result.
-    const double denom = reduction == 0 ? (double)(hdr->count > 0 ? hdr->count : 1) : 1.0;
+    const int64_t count = count_global ? *count_global : hdr->count;
+    const double denom = reduction == 0 ? (double)(count > 0 ? count : 1) : 1.0;
     const float loss = (hdr->status & kDevTimeout) ? __int_as_float(0x7fc00000) : (float)(red[0] / denom);
     hdr->loss = loss;
     hdr->scale = reduction == 2 ? 1.0f : (float)((double)grad_loss / denom);
@@ -858,7 +881,8 @@ static GemmParams base_params(const flce_problem& p, WsHeader* hdr) {
 // reduction: 0 mean, 1 sum, 2 none (per-row losses into loss_rows, `loss` unused).
 static flce_status run_forward(const flce_problem& p, const Plan& pl, const Maps& mp, const int64_t* y,
                                float* lse, float* loss, float grad_loss, uint8_t* ws, int sms, cudaStream_t st,
-                               const float* bias = nullptr, int reduction = 0, float* loss_rows = nullptr) {
+                               const float* bias = nullptr, int reduction = 0, float* loss_rows = nullptr,
+                               const int64_t* count_global = nullptr) {
   WsHeader* hdr = reinterpret_cast<WsHeader*>(ws);
   float* part_m = reinterpret_cast<float*>(ws + pl.off_pm);
   float* part_s = reinterpret_cast<float*>(ws + pl.off_ps);
@@ -901,7 +925,7 @@ static flce_status run_forward(const flce_problem& p, const Plan& pl, const Maps
   }
   const int n_blocks = (int)ceil_div(p.n_rows, kCombineRows);
   ProfScope prof(FLCE_KERNEL_FINALIZE, st);
-  finalize_kernel<<<1, 256, 0, st>>>(bsum, n_blocks, grad_loss, hdr, loss, reduction);
+  finalize_kernel<<<1, 256, 0, st>>>(bsum, n_blocks, grad_loss, hdr, loss, reduction, count_global);
   if (cudaGetLastError() != cudaSuccess) return FLCE_ERR_CUDA;
   return FLCE_OK;
 }
@@ -1407,9 +1431,11 @@ flce_status flce_forward(const flce_problem* p, const void* H, const void* W, co
                      static_cast<cudaStream_t>(stream));
 }
 
-flce_status flce_forward_backward(const flce_problem* p, const void* H, const void* W, const int64_t* y,
-                                  float grad_loss, float* lse, float* loss, float* dH, float* dW, void* ws,
-                                  size_t ws_bytes, void* stream) {
+// flce_forward_backward, and flce_forward_backward_global when count_global
+// is not NULL.
+static flce_status forward_backward_impl(const flce_problem* p, const void* H, const void* W, const int64_t* y,
+                                         const int64_t* count_global, float grad_loss, float* lse, float* loss,
+                                         float* dH, float* dW, void* ws, size_t ws_bytes, void* stream) {
   flce_status s = check_common(p, H, W, y, loss, ws, ws_bytes);
   if (s != FLCE_OK) return s;
   if (!dW || (p->n_rows > 0 && !dH)) return FLCE_ERR_INVALID_ARGUMENT;
@@ -1425,16 +1451,40 @@ flce_status flce_forward_backward(const flce_problem* p, const void* H, const vo
   if (p->n_rows == 0) {
     // No rows: loss 0 and dW = 0.
     Maps none;
-    flce_status r = run_forward(*p, pl, none, y, lse_buf, loss, grad_loss, wsb, sms, st);
+    flce_status r = run_forward(*p, pl, none, y, lse_buf, loss, grad_loss, wsb, sms, st, nullptr, 0, nullptr,
+                                count_global);
     if (r != FLCE_OK) return r;
     if (cudaMemsetAsync(dW, 0, (size_t)p->vocab * p->hidden * 4, st) != cudaSuccess) return FLCE_ERR_CUDA;
     return FLCE_OK;
   }
   Maps mp;
   if (!build_maps(*p, pl, H, W, dH, dW, wsb, true, &mp)) return FLCE_ERR_CUDA;
-  flce_status r = run_forward(*p, pl, mp, y, lse_buf, loss, grad_loss, wsb, sms, st);
+  flce_status r = run_forward(*p, pl, mp, y, lse_buf, loss, grad_loss, wsb, sms, st, nullptr, 0, nullptr,
+                              count_global);
   if (r != FLCE_OK) return r;
   return run_backward_any(*p, pl, mp, H, W, y, lse_buf, dH, dW, wsb, sms, st, nullptr, nullptr, nullptr);
+}
+
+flce_status flce_forward_backward(const flce_problem* p, const void* H, const void* W, const int64_t* y,
+                                  float grad_loss, float* lse, float* loss, float* dH, float* dW, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  return forward_backward_impl(p, H, W, y, nullptr, grad_loss, lse, loss, dH, dW, ws, ws_bytes, stream);
+}
+
+flce_status flce_count_valid(const flce_problem* p, const int64_t* y, int64_t* count, void* stream) {
+  if (!problem_ok(p) || !count || (p->n_rows > 0 && !y)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(y, 8) || !aligned(count, 8)) return FLCE_ERR_INVALID_ARGUMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ProfScope prof(FLCE_KERNEL_COUNT, st);
+  count_valid_kernel<<<1, 1024, 0, st>>>(y, p->n_rows, p->vocab, p->ignore_index, count);
+  return cudaGetLastError() == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
+}
+
+flce_status flce_forward_backward_global(const flce_problem* p, const void* H, const void* W, const int64_t* y,
+                                         const int64_t* count_global, float grad_loss, float* lse, float* loss,
+                                         float* dH, float* dW, void* ws, size_t ws_bytes, void* stream) {
+  if (!count_global || !aligned(count_global, 8)) return FLCE_ERR_INVALID_ARGUMENT;
+  return forward_backward_impl(p, H, W, y, count_global, grad_loss, lse, loss, dH, dW, ws, ws_bytes, stream);
 }
 
 static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {

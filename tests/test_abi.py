@@ -21,7 +21,8 @@ def test_library_exports_every_declared_symbol():
                              "flce_get_device_status", "flce_status_string", "flce_get_filter_stats",
                              "flce_profile_set", "flce_profile_count", "flce_forward_static_scratch",
                              "flce_forward_ex", "flce_backward_ex", "flce_forward_workspace_bytes",
-                             "flce_get_vocab_order", "flce_forward_backward_adamw", "flce_adamw_step"}
+                             "flce_get_vocab_order", "flce_forward_backward_adamw", "flce_adamw_step",
+                             "flce_count_valid", "flce_forward_backward_global"}
     out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
     for name in declared:
@@ -210,3 +211,19 @@ def test_api_refuses_cpu_tensors():
     y = torch.zeros(4, dtype=torch.int64)
     with pytest.raises(ValueError):
         flce.forward(H, W, y)
+
+
+def test_data_parallel_calls_reject_bad_arguments_on_the_host():
+    # Rejected before any launch, so this runs without a GPU.
+    p = flce.make_problem(64, 128, 1000)
+    nb = flce.flce_workspace_bytes(p)
+    assert flce.flce_count_valid(p, FAKE, None, stream=0) == Status.ERR_INVALID_ARGUMENT
+    assert flce.flce_count_valid(None, FAKE, FAKE, stream=0) == Status.ERR_INVALID_ARGUMENT
+    assert flce.flce_count_valid(p, FAKE + 4, FAKE, stream=0) == Status.ERR_INVALID_ARGUMENT
+    call = flce.flce_forward_backward_global
+    assert call(p, FAKE, FAKE, FAKE, None, 1.0, None, FAKE, FAKE, FAKE, FAKE, ws_bytes=nb,
+                stream=0) == Status.ERR_INVALID_ARGUMENT
+    assert call(p, FAKE, FAKE, FAKE, FAKE + 4, 1.0, None, FAKE, FAKE, FAKE, FAKE, ws_bytes=nb,
+                stream=0) == Status.ERR_INVALID_ARGUMENT
+    assert call(p, FAKE, FAKE, FAKE, FAKE, 1.0, None, FAKE, FAKE, FAKE, FAKE, ws_bytes=nb - 1,
+                stream=0) == Status.ERR_WORKSPACE_TOO_SMALL

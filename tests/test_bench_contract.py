@@ -26,6 +26,7 @@ def test_reference_arm_prints_one_contract_line():
     assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
     assert d["value"] > 0 and d["config"]["workload"] == "tiny" and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["uname_m"] and d["cpu_baseline"]["cpu_model"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
 
 
