@@ -74,13 +74,15 @@ def test_static_scratch_matches_the_oracle():
 
 def test_static_scratch_reports_a_timed_out_forward_as_nan_loss():
     # With every bounded wait cut to about a microsecond the forward GEMM
-    # gives up; with no workspace to query, the NaN loss is the report. The
-    # next call starts from a clean scratch and matches flce_forward.
-    inp = small_inputs(512, 256, 4096, seed=11)
+    # gives up: with D = 4096 each tile's accumulator takes 64 k-blocks (over
+    # 30,000 SM cycles) of MMAs, so the epilogue's first wait cannot end in
+    # time. With no workspace to query, the NaN loss is the report. The next
+    # call starts from a clean scratch and matches flce_forward.
+    inp = small_inputs(512, 4096, 4096, seed=11)
     H, W, y = to_device(inp)
-    loss, _ = _static(flce.make_problem(512, 256, 4096, flags=flce.FLAG_TEST_SHORT_WAITS), H, W, y)
+    loss, _ = _static(flce.make_problem(512, 4096, 4096, flags=flce.FLAG_TEST_SHORT_WAITS), H, W, y)
     assert np.isnan(loss)
-    prob = flce.make_problem(512, 256, 4096)
+    prob = flce.make_problem(512, 4096, 4096)
     ref_loss, ref_lse = _with_workspace(prob, H, W, y)
     loss, lse = _static(prob, H, W, y)
     assert abs(loss - ref_loss) <= LOSS_REL * abs(ref_loss)
