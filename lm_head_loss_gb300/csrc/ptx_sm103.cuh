@@ -33,6 +33,21 @@ __device__ __forceinline__ uint32_t elect_one_lane() {
   return pred;
 }
 
+// The value itself, through a move the compiler cannot see into: the result
+// lives in a register, so a loop that uses it does not re-read the memory
+// (kernel parameters) it came from after each asm statement with a memory
+// clobber.
+__device__ __forceinline__ int32_t pin(int32_t v) {
+  int32_t r;
+  asm volatile("mov.b32 %0, %1;" : "=r"(r) : "r"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t pin(uint64_t v) {
+  uint64_t r;
+  asm volatile("mov.b64 %0, %1;" : "=l"(r) : "l"(v));
+  return r;
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
@@ -310,6 +325,17 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];"
       ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar_cluster_addr)
+      : "memory");
+}
+
+// The same copy with the shared-memory destination as a shared-window
+// address and the tensor map as a generic address, both already in registers.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t smem_dst, uint64_t tmap, int32_t c0, int32_t c1,
+                                                 uint32_t bar_cluster_addr) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_dst), "l"(tmap), "r"(c0), "r"(c1), "r"(bar_cluster_addr)
       : "memory");
 }
 

@@ -124,47 +124,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
       const uint32_t full_leader = ptx::map_to_rank(&full_bar[0], 0);
-      uint32_t stage = 0, phase = 0;
-      int32_t last_parity[kStg];
-      for (int s = 0; s < kStg; ++s) last_parity[s] = -1;
+      const uint32_t smem_base = ptx::smem_u32(smem);
+      uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
       const TileOrder ord(unit0, unit_stride, num_tiles, L.order_groups);
       for (int j = 0; j < ord.count && ok; ++j) {
         int pi, mt, nt;
         const int tl = decode_tile(L, ord.tile(j), pi);
         const GemmParams& p = L.prob[pi];
-        const CUtensorMap* tmA = &L.tm_a[pi];
-        const CUtensorMap* tmB = &L.tm_b[pi];
         tile_coords(p, tl, 2, rank, mt, nt);
         const bool may_skip = kSkip && p.skip_by_flags != 0;
         const uint64_t keep = may_skip ? tile_keep(p, mt - rank, 2) : ~0ull;
-        const int k_blocks = p.k_blocks;
+        // Everything the k-loop needs, read from the parameters once per tile
+        // and pinned in registers: the single producer thread issues a TMA
+        // copy every few hundred cycles, and re-reading parameters between
+        // the copies measurably slowed the whole pipeline.
+        const uint64_t tmA = ptx::pin(reinterpret_cast<uint64_t>(&L.tm_a[pi]));
+        const uint64_t tmB = ptx::pin(reinterpret_cast<uint64_t>(&L.tm_b[pi]));
+        const int32_t a_mn = ptx::pin(p.a_mn), b_mn = ptx::pin(p.b_mn);
+        const int32_t a_m = ptx::pin(p.a_m0 + mt * kBM), a_k = ptx::pin(p.a_k0);
+        const int32_t b_n = ptx::pin(p.b_n0 + nt * kBN + rank * (kBN / 2)), b_k = ptx::pin(p.b_k0);
+        const int32_t k_blocks = ptx::pin(p.k_blocks);
+        const int32_t unit_kb = kSkip ? ptx::pin(p.flags_a_is_rows ? kBN / kBK : kBM / kBK) : 1;
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (kSkip && may_skip && kblock_dropped(p, keep, kb)) continue;
+          if (kSkip && may_skip && ((keep >> (kb / unit_kb)) & 1ull) == 0ull) continue;
           if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
             break;
           }
-          uint8_t* sa = smem + stage * kPairStageBytes;
-          uint8_t* sb = sa + kABytes;
+          const uint32_t sa = smem_base + stage * kPairStageBytes;
+          const uint32_t sb = sa + kABytes;
           const uint32_t fb = full_leader + stage * 8u;
           if (leader) ptx::mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
           const int32_t kc = kb * kBK;
-          if (p.a_mn) {
-            for (int h = 0; h < kBM / 64; ++h)
-              ptx::tma_load_2d_pair(sa + h * 8192, tmA, p.a_m0 + mt * kBM + h * 64, p.a_k0 + kc, fb);
+          if (a_mn) {
+            ptx::tma_load_2d_pair(sa, tmA, a_m, a_k + kc, fb);
+            ptx::tma_load_2d_pair(sa + 8192, tmA, a_m + 64, a_k + kc, fb);
           } else {
-            ptx::tma_load_2d_pair(sa, tmA, p.a_k0 + kc, p.a_m0 + mt * kBM, fb);
+            ptx::tma_load_2d_pair(sa, tmA, a_k + kc, a_m, fb);
           }
-          const int32_t n_half = p.b_n0 + nt * kBN + rank * (kBN / 2);
-          if (p.b_mn) {
-            for (int h = 0; h < (kBN / 2) / 64; ++h)
-              ptx::tma_load_2d_pair(sb + h * 8192, tmB, n_half + h * 64, p.b_k0 + kc, fb);
+          if (b_mn) {
+            ptx::tma_load_2d_pair(sb, tmB, b_n, b_k + kc, fb);
+            ptx::tma_load_2d_pair(sb + 8192, tmB, b_n + 64, b_k + kc, fb);
           } else {
-            ptx::tma_load_2d_pair(sb, tmB, p.b_k0 + kc, n_half, fb);
+            ptx::tma_load_2d_pair(sb, tmB, b_k + kc, b_n, fb);
           }
-          last_parity[stage] = (int32_t)phase;
+          ++issued;
           if (++stage == kStg) {
             stage = 0;
             phase ^= 1u;
@@ -174,9 +180,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
       if (!ok && leader) {
         // The even CTA's full barriers count both CTAs' bytes: once a phase
         // completes, no copy of that phase is still landing in either CTA.
+        // Stage s was last filled in the current phase if s < stage, in the
+        // previous one otherwise (if `issued` ever reached it).
         volatile uint32_t never = 0u;
-        for (int s = 0; s < kStg; ++s)
-          if (last_parity[s] >= 0) ptx::mbar_wait_bounded(&full_bar[s], (uint32_t)last_parity[s], 100000000ull, &never);
+        for (uint32_t s = 0; s < (uint32_t)kStg; ++s)
+          if (s < issued) ptx::mbar_wait_bounded(&full_bar[s], s < stage ? phase : (phase ^ 1u), 100000000ull, &never);
       }
     }
     __syncwarp();
@@ -199,7 +207,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
         // epilogue writes it without reading TMEM, and both sides skip the
         // hand-off for it.
         if (kSkip && may_skip && keep == 0ull) continue;
-        const uint32_t idesc = ptx::idesc_bf16_f32(2 * kBM, kBN, p.a_mn != 0, p.b_mn != 0);
+        const uint32_t idesc = (uint32_t)ptx::pin((int32_t)ptx::idesc_bf16_f32(2 * kBM, kBN, p.a_mn != 0, p.b_mn != 0));
         const uint32_t buf = i & 1, use = i >> 1;
         ++i;
         if (!ptx::mbar_wait_bounded(&acc_empty[buf], (use & 1u) ^ 1u, wait_limit_ns, abort_flag)) {
@@ -210,8 +218,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * kBN;
         uint32_t accumulate = 0;
-        const bool a_mn = p.a_mn != 0, b_mn = p.b_mn != 0;
-        const int k_blocks = p.k_blocks;
+        const bool a_mn = ptx::pin(p.a_mn) != 0, b_mn = ptx::pin(p.b_mn) != 0;
+        const int k_blocks = ptx::pin(p.k_blocks);
         for (int kb = 0; kb < k_blocks; ++kb) {
           if (kSkip && may_skip && kblock_dropped(p, keep, kb)) continue;
           if (!ptx::mbar_wait_bounded(&full_bar[stage], phase, wait_limit_ns, abort_flag)) {
