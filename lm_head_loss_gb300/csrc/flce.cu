@@ -822,6 +822,16 @@ static int adamw_order_groups() {
   return groups;
 }
 
+// Programmatic dependent launch of the pair GEMM (FLCE_PDL=0 switches it
+// off, for comparisons).
+static bool programmatic_launch() {
+  static const bool on = [] {
+    const char* e = std::getenv("FLCE_PDL");
+    return !(e && std::strcmp(e, "0") == 0);
+  }();
+  return on;
+}
+
 static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
   if (g.units <= 0) return true;
   ProfScope prof(kind, st);
@@ -836,13 +846,18 @@ static bool launch_group(int kind, const Group& g, int sms, cudaStream_t st) {
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // Programmatic dependent launch: this launch's prologue may overlap the
+  // tail of the previous kernel in the stream; the kernel waits for it
+  // (griddepcontrol.wait) before touching global memory.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = programmatic_launch() ? 2 : 1;
   bool skip = false;
   int modes = 0;
   for (int q = 0; q < g.L.n_probs; ++q) {

@@ -48,6 +48,14 @@ __device__ __forceinline__ uint64_t pin(uint64_t v) {
   return r;
 }
 
+// Programmatic dependent launch. launch_dependents lets the next kernel in
+// the stream (launched with programmatic stream serialization) begin its
+// prologue once every CTA of this grid has issued it or exited;
+// wait_prior_grids blocks until the grids this one depends on have
+// completed and their memory operations are visible.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_prior_grids() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

@@ -119,6 +119,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
   ptx::cluster_sync_all();                          // both CTAs' barriers exist
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The prologue above touches only shared memory, TMEM and the kernel
+  // parameters, so it may overlap the end of the previous GEMM launch (which
+  // may have written this launch's operands): every thread waits for that
+  // launch before its first global-memory access. The next launch may start
+  // its own prologue as soon as an SM frees up.
+  ptx::wait_prior_grids();
+  if (threadIdx.x == 0) ptx::launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
