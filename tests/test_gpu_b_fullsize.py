@@ -25,10 +25,10 @@ N_SAMPLE_ROWS = 256
 N_SAMPLE_VOCAB = 256
 
 
-def _run(inp, filter_eps=0.0):
+def _run(inp, filter_eps=0.0, flags=0):
     H, W, y = to_device(inp)
     ws = flce.Workspace(H.device)
-    loss, lse, dH, dW = flce.forward_backward(H, W, y, workspace=ws, filter_eps=filter_eps)
+    loss, lse, dH, dW = flce.forward_backward(H, W, y, workspace=ws, filter_eps=filter_eps, flags=flags)
     st = flce.device_status(ws)
     out = {"loss": loss.item(), "lse": lse.cpu().numpy(), "dH": dH.cpu().numpy(), "dW": dW.cpu().numpy(),
            "status": st}
@@ -120,6 +120,41 @@ def test_full_size_gemma_filter_off_and_on():
     print("gemma filter on", r_on, "skipped tile fraction", on["skipped"])
     assert on["loss"] == off["loss"]
     assert r_on["dH_rel_sampled"] <= 5e-2 and r_on["dW_rel_sampled"] <= 5e-2
+
+
+def test_full_size_gemma_filter_variants_report():
+    # The filtered variants at the Gemma-2-2B head itself (N=8192, D=2304,
+    # V=256000, eps = 2^-12; Cut Cross-Entropy Sec. 4.3 "Gradient filtering"
+    # and Table 1): the skipped tile fraction and the error of dH and dW
+    # against the unfiltered oracle on the sampled rows and ids, as max
+    # absolute error (relative to max|ref|) and relative Frobenius error.
+    inp = synth.make_inputs(synth.WORKLOADS["gemma2_2b_head"], seed=0)
+    H64, W64 = oracle.inputs_f64(inp["H"], inp["W"])
+    y = inp["y"]
+    rows, vocab = _samples(inp, 0)
+    lse, _, _ = oracle.forward(H64, W64, y)
+    dH_ref = oracle.dH_rows(H64, W64, y, rows)
+    dW_ref = oracle.dW_rows(H64, W64, y, lse, vocab)
+
+    def err(got, ref):
+        d = got.astype(np.float64) - ref
+        return {"max_abs_rel": float(np.max(np.abs(d)) / np.max(np.abs(ref))),
+                "frobenius_rel": float(np.linalg.norm(d) / np.linalg.norm(ref))}
+
+    variants = {"off": (0.0, 0), "both": (2.0 ** -12, 0), "full_dw (CCE-FullC)": (2.0 ** -12, flce.FLAG_FILTER_FULL_DW),
+                "both + sorted vocabulary": (2.0 ** -12, flce.FLAG_SORT_VOCAB)}
+    report = {}
+    for name, (eps, flags) in variants.items():
+        got = _run(inp, filter_eps=eps, flags=flags)
+        assert got["status"] == flce.Status.OK
+        report[name] = {"skipped_tile_fraction": got.get("skipped", 0.0), "dH": err(got["dH"][rows], dH_ref),
+                        "dW": err(got["dW"][vocab], dW_ref)}
+        if eps == 0.0:
+            _assert_report({"dH_rel": report[name]["dH"]["max_abs_rel"], "dW_rel": report[name]["dW"]["max_abs_rel"]})
+        else:
+            assert report[name]["dH"]["max_abs_rel"] <= 5e-2 and report[name]["dW"]["max_abs_rel"] <= 5e-2, report
+    import json
+    print("FILTER_REPORT", json.dumps(report))
 
 
 def test_full_size_long_context_131072_rows():
