@@ -404,72 +404,87 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
     const float sc = __ldg(p.scale);
     if ((kModes & kModeAdamw) && p.mode == EPI_ADAMW) {
       // AdamW on the finished gradient tile (the FORGE explainer's fused
-      // optimizer): one thread per weight row, 32 columns at a time, rows
-      // through out_rows when the vocabulary runs in sorted order. The 24
-      // loads of a slice are issued before the accumulator is read, so the
-      // memory latency overlaps the TMEM read and the other warps' work.
+      // optimizer), 32 columns at a time. The accumulator gives each thread
+      // one row; the slice goes through this warp's shared-memory box so that
+      // the weights and moments are read and written row by row instead:
+      // lane (rs, j) handles columns 4j..4j+3 of rows rs, rs + 4, ..., rs + 28
+      // of the warp's 32, and one warp instruction covers four whole 128-byte
+      // lines of each array. (With one row per thread every instruction
+      // touched 32 lines, which the small L1 left beside the 230 KiB of
+      // shared memory could not hold.) Rows go through out_rows when the
+      // vocabulary runs in sorted order. The loads of a slice are issued
+      // before the accumulator is read.
       float oc[kAdamwConsts];
 #pragma unroll
       for (int i = 0; i < kAdamwConsts; ++i) oc[i] = __ldg(p.opt + i);
-      const int srow = p.out_m0 + lrow;
-      const bool row_ok = lrow < p.m_valid && srow < p.out_rows_n;
-      const int64_t drow = row_ok ? (p.out_rows ? (int64_t)__ldg(p.out_rows + srow) : (int64_t)srow) : 0;
-      float* __restrict__ prow = p.out_ptr + drow * p.out_ld;
-      float* __restrict__ mrow = p.opt_m + drow * p.out_ld;
-      float* __restrict__ vrow = p.opt_v + drow * p.out_ld;
-      __nv_bfloat16* __restrict__ wrow = p.opt_w + drow * p.out_ld;
+      // An earlier tile's TMA stores may still be reading the boxes.
+      if (lane == 0) ptx::bulk_wait_group_read<0>();
+      __syncwarp();
+      const int rs = lane >> 3, jc = lane & 7;
+      const int row_base = mt * kBM + q * 32;    // local row of the warp's row 0
+      int64_t drow[8];
+      bool rok[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int lr = row_base + rs + 4 * k;
+        const int sr = p.out_m0 + lr;
+        rok[k] = lr < p.m_valid && sr < p.out_rows_n;
+        drow[k] = rok[k] ? (p.out_rows ? (int64_t)__ldg(p.out_rows + sr) : (int64_t)sr) * p.out_ld : 0;
+      }
 #pragma unroll 1
       for (int c = 0; c < kBN; c += 32) {
-        const int c0 = nt * kBN + c;             // out_cols is a multiple of 8
+        const int col = nt * kBN + c + 4 * jc;   // out_cols is a multiple of 8, so 4 columns are all in or out
+        const bool col_ok = col < p.out_cols;
         float4 pv[8], mv[8], vv[8];
-        if (row_ok) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (c0 + 4 * j < p.out_cols) {
-              pv[j] = *reinterpret_cast<const float4*>(prow + c0 + 4 * j);
-              mv[j] = *reinterpret_cast<const float4*>(mrow + c0 + 4 * j);
-              vv[j] = *reinterpret_cast<const float4*>(vrow + c0 + 4 * j);
-            }
+        for (int k = 0; k < 8; ++k) {
+          if (rok[k] && col_ok) {
+            pv[k] = *reinterpret_cast<const float4*>(p.out_ptr + drow[k] + col);
+            mv[k] = *reinterpret_cast<const float4*>(p.opt_m + drow[k] + col);
+            vv[k] = *reinterpret_cast<const float4*>(p.opt_v + drow[k] + col);
           }
         }
-        float x[32];
-        if (all_skipped) {
+        uint8_t* sbox = my_boxes + ebuf * kEpiBoxBytes;
+        {
+          float x[32];
+          if (all_skipped) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = 0.f;
-        } else {
-          uint32_t r[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c, r);
-          ptx::tmem_ld_wait();
+            for (int j = 0; j < 32; ++j) x[j] = 0.f;
+          } else {
+            uint32_t r[32];
+            ptx::tmem_ld_32x32b_x32(taddr + c, r);
+            ptx::tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * sc;
+            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * sc;
+          }
+          // row `lane`, 16-byte chunk v at chunk v ^ (lane & 7)
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<float4*>(sbox + lane * 128 + ((v ^ (lane & 7)) * 16)) =
+                make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
         }
-        if (!row_ok) continue;
-        uint32_t wb[16];
+        __syncwarp();
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          float* pe = &pv[j].x;
-          float* me = &mv[j].x;
-          float* ve = &vv[j].x;
+        for (int k = 0; k < 8; ++k) {
+          const int r = rs + 4 * k;
+          const float4 g4 = *reinterpret_cast<const float4*>(sbox + r * 128 + ((jc ^ (r & 7)) * 16));
+          if (!(rok[k] && col_ok)) continue;
+          float* pe = &pv[k].x;
+          float* me = &mv[k].x;
+          float* ve = &vv[k].x;
+          const float g[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) adamw_update(oc, x[4 * j + e], pe[e], me[e], ve[e]);
+          for (int e = 0; e < 4; ++e) adamw_update(oc, g[e], pe[e], me[e], ve[e]);
+          *reinterpret_cast<float4*>(p.out_ptr + drow[k] + col) = pv[k];
+          *reinterpret_cast<float4*>(p.opt_m + drow[k] + col) = mv[k];
+          *reinterpret_cast<float4*>(p.opt_v + drow[k] + col) = vv[k];
           __nv_bfloat162 lo = __floats2bfloat162_rn(pe[0], pe[1]), hi = __floats2bfloat162_rn(pe[2], pe[3]);
-          wb[2 * j] = *reinterpret_cast<uint32_t*>(&lo);
-          wb[2 * j + 1] = *reinterpret_cast<uint32_t*>(&hi);
+          *reinterpret_cast<uint2*>(p.opt_w + drow[k] + col) =
+              make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (c0 + 4 * j < p.out_cols) {
-            *reinterpret_cast<float4*>(prow + c0 + 4 * j) = pv[j];
-            *reinterpret_cast<float4*>(mrow + c0 + 4 * j) = mv[j];
-            *reinterpret_cast<float4*>(vrow + c0 + 4 * j) = vv[j];
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (c0 + 8 * q < p.out_cols)
-            *reinterpret_cast<uint4*>(wrow + c0 + 8 * q) = make_uint4(wb[4 * q], wb[4 * q + 1], wb[4 * q + 2],
-                                                                      wb[4 * q + 3]);
+        ebuf ^= 1u;                              // the next slice writes the other box
       }
+      __syncwarp();
     } else if (p.out_rows) {
       // Row-mapped output (a vocabulary visited in sorted order writes dW
       // rows back in id order): one thread per row, 128 contiguous bytes
