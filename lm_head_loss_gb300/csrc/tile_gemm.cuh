@@ -487,39 +487,63 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, const CUtenso
       __syncwarp();
     } else if (p.out_rows) {
       // Row-mapped output (a vocabulary visited in sorted order writes dW
-      // rows back in id order): one thread per row, 128 contiguous bytes
-      // per 32-column slice. The map is a permutation of the output rows.
-      const int srow = p.out_m0 + lrow;
-      const bool row_ok = lrow < p.m_valid && srow < p.out_rows_n;
-      float* orow = p.out_ptr + (row_ok ? (int64_t)__ldg(p.out_rows + srow) * p.out_ld : 0);
+      // rows back in id order; the map is a permutation of the output rows).
+      // As in the AdamW epilogue, each 32-column slice goes through the
+      // warp's shared-memory box, so that lane (rs, j) writes columns
+      // 4j..4j+3 of rows rs, rs + 4, ..., rs + 28 and one instruction covers
+      // four whole 128-byte lines.
       if (!(all_skipped && p.mode == EPI_REDUCE)) {
+        if (lane == 0) ptx::bulk_wait_group_read<0>();   // earlier TMA stores may still read the boxes
+        __syncwarp();
+        const int rs = lane >> 3, jc = lane & 7;
+        const int row_base = mt * kBM + q * 32;
+        int64_t drow[8];
+        bool rok[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int lr = row_base + rs + 4 * k;
+          const int sr = p.out_m0 + lr;
+          rok[k] = lr < p.m_valid && sr < p.out_rows_n;
+          drow[k] = rok[k] ? (int64_t)__ldg(p.out_rows + sr) * p.out_ld : 0;
+        }
 #pragma unroll 1
         for (int c = 0; c < kBN; c += 32) {
-          float x[32];
-          if (all_skipped) {
+          uint8_t* sbox = my_boxes + ebuf * kEpiBoxBytes;
+          {
+            float x[32];
+            if (all_skipped) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = 0.f;
-          } else {
-            uint32_t r[32];
-            ptx::tmem_ld_32x32b_x32(taddr + c, r);
-            ptx::tmem_ld_wait();
+              for (int j = 0; j < 32; ++j) x[j] = 0.f;
+            } else {
+              uint32_t r[32];
+              ptx::tmem_ld_32x32b_x32(taddr + c, r);
+              ptx::tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * sc;
+              for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(r[j]) * sc;
+            }
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              *reinterpret_cast<float4*>(sbox + lane * 128 + ((v ^ (lane & 7)) * 16)) =
+                  make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
           }
-          const int col = nt * kBN + c;
-          if (row_ok) {
+          __syncwarp();
+          const int col = nt * kBN + c + 4 * jc;
+          if (col < p.out_cols) {
 #pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              const int cc = col + 4 * v;
-              if (cc < p.out_cols) {
-                if (p.mode == EPI_REDUCE)
-                  ptx::red_add_v4(orow + cc, x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
-                else
-                  *reinterpret_cast<float4*>(orow + cc) = make_float4(x[4 * v], x[4 * v + 1], x[4 * v + 2], x[4 * v + 3]);
-              }
+            for (int k = 0; k < 8; ++k) {
+              if (!rok[k]) continue;
+              const int r = rs + 4 * k;
+              const float4 g4 = *reinterpret_cast<const float4*>(sbox + r * 128 + ((jc ^ (r & 7)) * 16));
+              float* dst = p.out_ptr + drow[k] + col;
+              if (p.mode == EPI_REDUCE)
+                ptx::red_add_v4(dst, g4.x, g4.y, g4.z, g4.w);
+              else
+                *reinterpret_cast<float4*>(dst) = g4;
             }
           }
+          ebuf ^= 1u;
         }
+        __syncwarp();
       }
     } else if (!(all_skipped && p.mode == EPI_REDUCE)) {
 #pragma unroll 1
