@@ -66,3 +66,61 @@ def test_single_process_data_parallel_step_is_the_plain_call():
     assert torch.equal(dH, ref_dH) and torch.equal(dW, ref_dW)
     assert_parity({"loss": float(loss.item()), "lse": lse.cpu().numpy(), "dH": dH.cpu().numpy(),
                    "dW": dW.cpu().numpy()}, oracle_full(inp))
+
+
+# Two processes on the one GPU, each a rank of a gloo process group (NCCL takes
+# one rank per GPU). Each rank runs DataParallelStep on its own rows; the
+# all-reduces go through torch.distributed on the host, so no rank's kernels
+# wait on the other's. The result must equal the oracle on the whole batch.
+_DP_SHAPE = (900, 256, 6000, 350)   # rows, hidden, vocab, rows of rank 0
+
+
+def _dp_rank(rank, world, port, q):
+    import os
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.cuda.set_device(0)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        n, d, v, split = _DP_SHAPE
+        inp = small_inputs(n, d, v, seed=77, targets="zipf", ignore=0.1)
+        H, W, y = to_device(inp)
+        rows = slice(0, split) if rank == 0 else slice(split, n)
+        Hr, yr = H[rows].contiguous(), y[rows].contiguous()
+        step = flce.DataParallelStep(Hr.shape[0], d, v, "cuda")
+        loss, lse, dH, dW, count = step(Hr, W, yr, grad_loss=0.75)
+        torch.cuda.synchronize()
+        assert step.device_status() == flce.Status.OK
+        q.put((rank, float(loss.item()), lse.cpu().numpy(), dH.cpu().numpy(), dW.cpu().numpy(), int(count.item())))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_process_data_parallel_step_matches_the_whole_batch():
+    import socket
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_dp_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = {}
+    for _ in range(2):
+        r = q.get(timeout=300)
+        got[r[0]] = r
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    n, d, v, split = _DP_SHAPE
+    inp = small_inputs(n, d, v, seed=77, targets="zipf", ignore=0.1)
+    ref = oracle_full(inp, grad_loss=0.75)
+    assert got[0][5] == got[1][5] == ref["count"]
+    for rank in (0, 1):
+        assert got[rank][1] == got[0][1]                        # every rank holds the global loss
+        assert np.array_equal(got[rank][4], got[0][4])          # and the same summed dW
+    whole = {"loss": got[0][1], "lse": np.concatenate([got[0][2], got[1][2]]),
+             "dH": np.concatenate([got[0][3], got[1][3]]), "dW": got[0][4]}
+    print("two processes vs whole batch", assert_parity(whole, ref))
