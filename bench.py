@@ -126,7 +126,7 @@ def recorded_traffic(workload: str):
         return None, "DRAM capture recorded for another workload"
     if rec.get("kernel_sources_sha256") != kernel_sources_sha256():
         return None, "kernel sources changed since the DRAM capture"
-    return float(rec["dram_bytes_per_gemm_launch"]) / 1e9, rec.get("command", "")
+    return float(rec["dram_bytes_per_gemm_launch"]) / 1e9, rec.get("command") or "; ".join(rec.get("commands", []))
 
 
 def gemm_kernel_name() -> str:
