@@ -123,11 +123,12 @@ __global__ void count_valid_kernel(const int64_t* __restrict__ y, int64_t n, int
 }
 
 // Merge of the per-tile (max, sum) partials into LSE_n. A block covers 32
-// rows; thread (r, g) merges tiles g, g + 8, g + 16, ... of row r, then the 8
-// partials of a row are merged in g order and the 32 row losses of the block
-// are summed in a fixed tree order (fp64).
+// rows; thread (r, g) merges tiles g, g + 32, g + 64, ... of row r, then the
+// 32 partials of a row are merged in g order and the 32 row losses of the
+// block are summed in a fixed order (fp64). 1024 threads per block keep
+// enough loads in flight to read the partials near HBM speed.
 constexpr int kCombineRows = 32;
-constexpr int kCombineSplit = 8;
+constexpr int kCombineSplit = 32;
 
 __device__ __forceinline__ void lse_merge(float& mx, float& sm, float m, float s) {
   if (m > mx) {
