@@ -40,3 +40,26 @@ def test_source_digest_ignores_comments_only(tmp_path, monkeypatch):
     assert bench.kernel_sources_sha256() == base
     (csrc / "k.cu").write_text("__global__ void k() { int a = 2; }\n")
     assert bench.kernel_sources_sha256() != base
+
+
+def test_phase_fractions_split_the_gemm_time():
+    # 2NVD over the forward GEMM, 6NVD over the recompute and grouped launches,
+    # each as a fraction of the given peak; with the filter on, the backward
+    # counts the lower bound of the FLOPs it executed.
+    n, d, v, steps = 8192, 2048, 151552, 10
+    per_kind = {"gemm_lse": {"ms": 26.0, "launches": 10}, "gemm_dz": {"ms": 1.6, "launches": 10},
+                "gemm_bwd": {"ms": 86.0, "launches": 180}, "combine": {"ms": 0.2, "launches": 10}}
+    out = bench.phase_fractions(per_kind, steps, n, d, v, peak=2000.0, skipped=None)
+    fwd_tf = 2.0 * n * v * d / 2.6e-3 / 1e12
+    bwd_tf = 6.0 * n * v * d / 8.76e-3 / 1e12
+    assert abs(out["forward"]["tflops"] - fwd_tf) < 1e-6 * fwd_tf
+    assert abs(out["backward"]["tflops"] - bwd_tf) < 1e-6 * bwd_tf
+    assert abs(out["forward"]["frac"] - fwd_tf / 2000.0) < 1e-9
+    half = bench.phase_fractions(per_kind, steps, n, d, v, peak=2000.0, skipped=0.5)
+    assert abs(half["backward"]["tflops"] - bwd_tf * 4.0 / 6.0) < 1e-6 * bwd_tf
+    assert bench.phase_fractions({}, steps, n, d, v, 2000.0, None)["forward"]["frac"] is None
+
+
+def test_host_cpu_names_architecture_and_model():
+    info = bench.host_cpu()
+    assert info["uname_m"] and isinstance(info["cpu_model"], str) and info["cpu_model"]
