@@ -267,6 +267,10 @@ def run_ours(args, rank, world, local):
     H = torch.from_numpy(inp["H"].view(np.int16)).view(torch.bfloat16).to(dev)
     W = torch.from_numpy(inp["W"].view(np.int16)).view(torch.bfloat16).to(dev)
     y = torch.from_numpy(inp["y"]).to(dev)
+    if world > 1:
+        # Data parallel: each rank has its own rows but the one W (rank 0's).
+        dist.broadcast(W, src=0)
+        inp["W"] = W.cpu().view(torch.int16).numpy().view(np.uint16)
     flags = ((flce.FLAG_COMPACT_IGNORED if args.compact_ignored else 0) | (flce.FLAG_SORT_VOCAB if args.sort_vocab else 0)
              | (flce.FLAG_FILTER_FULL_DW if args.filter_full_dw else 0)
              | (flce.FLAG_FILTER_FULL_DH if args.filter_full_dh else 0))
@@ -419,6 +423,8 @@ def run_ours(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "n_rows": N, "hidden": D, "vocab": V, "global_batch_rows": N * world,
+                   "batch_per_rank": "own rows (H, y) drawn with seed + rank; W drawn with the seed, the same on "
+                                     "every rank" if world > 1 else "one batch",
                    "targets": wl.targets, "ignore_frac": wl.ignore_frac, "filter_eps": args.filter_eps,
                    "compact_ignored": bool(args.compact_ignored), "sort_vocab": bool(args.sort_vocab),
                    "filter_variant": ("full_dw (CCE-FullC)" if args.filter_full_dw else
@@ -614,7 +620,14 @@ def main():
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        # NCCL between the GPUs of one node; FLCE_DIST_BACKEND=gloo runs the same
+        # ranks with host-side collectives (a check of the multi-rank path when
+        # the ranks share a GPU: no kernel of one rank waits on another's).
+        backend = os.environ.get("FLCE_DIST_BACKEND", "nccl")
+        if backend == "nccl":
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
     result = run_ours(args, rank, world, local)
     if rank == 0:
         print(json.dumps(result), flush=True)
