@@ -152,9 +152,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
         const int32_t a_m = ptx::pin(p.a_m0 + mt * kBM), a_k = ptx::pin(p.a_k0);
         const int32_t b_n = ptx::pin(p.b_n0 + nt * kBN + rank * (kBN / 2)), b_k = ptx::pin(p.b_k0);
         const int32_t k_blocks = ptx::pin(p.k_blocks);
-        const int32_t unit_kb = kSkip ? ptx::pin(p.flags_a_is_rows ? kBN / kBK : kBM / kBK) : 1;
+        // k-block kb reads keep-mask unit kb >> unit_shift (a dH unit spans
+        // 256 staging columns = 4 k-blocks, a dW unit 128 rows = 2): a shift,
+        // since a division by a pinned value would be a software division
+        // on every k-block.
+        static_assert(kBN / kBK == 4 && kBM / kBK == 2, "keep-mask units of 4 and 2 k-blocks");
+        const int32_t unit_shift = kSkip ? ptx::pin(p.flags_a_is_rows ? 2 : 1) : 0;
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (kSkip && may_skip && ((keep >> (kb / unit_kb)) & 1ull) == 0ull) continue;
+          if (kSkip && may_skip && ((keep >> (kb >> unit_shift)) & 1ull) == 0ull) continue;
           if (!ptx::mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
@@ -227,8 +232,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
         uint32_t accumulate = 0;
         const bool a_mn = ptx::pin(p.a_mn) != 0, b_mn = ptx::pin(p.b_mn) != 0;
         const int k_blocks = ptx::pin(p.k_blocks);
+        const int32_t unit_shift = kSkip ? ptx::pin(p.flags_a_is_rows ? 2 : 1) : 0;   // as in the producer
         for (int kb = 0; kb < k_blocks; ++kb) {
-          if (kSkip && may_skip && kblock_dropped(p, keep, kb)) continue;
+          if (kSkip && may_skip && ((keep >> (kb >> unit_shift)) & 1ull) == 0ull) continue;
           if (!ptx::mbar_wait_bounded(&full_bar[stage], phase, wait_limit_ns, abort_flag)) {
             record_timeout(status, abort_flag);
             ok = false;
