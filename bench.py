@@ -146,16 +146,25 @@ def measured_peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples every 100 ms while the timed region runs."""
+    """nvidia-smi samples every 50 ms. The sampler is running before the timed
+    region starts (the first sample has arrived), and the summary keeps the
+    samples whose timestamps fall between mark_start() and mark_end()."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
+    # NVML's clocks-event reason bits, as nvidia-smi prints them in clocks_event_reasons.active.
+    REASON_BITS = ((0x1, "gpu_idle"), (0x2, "applications_clocks_setting"), (0x4, "sw_power_cap"),
+                   (0x8, "hw_slowdown"), (0x10, "sync_boost"), (0x20, "sw_thermal_slowdown"),
+                   (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"),
+                   (0x100, "display_clock_setting"))
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -163,14 +172,26 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", str(self.PERIOD_MS)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
-        time.sleep(0.3)
+        deadline = time.time() + 5.0
+        while self.proc is not None and time.time() < deadline and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
+        time.sleep(2 * self.PERIOD_MS / 1000.0)
         return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __exit__(self, *exc):
         if self.proc is not None:
+            time.sleep(self.PERIOD_MS / 1000.0)
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -178,32 +199,69 @@ class ClockSampler:
                 self.proc.kill()
         return False
 
+    @staticmethod
+    def _stamp(text: str):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                continue
+        return None
+
+    @classmethod
+    def _active_names(cls, field: str):
+        try:
+            mask = int(field, 16)
+        except ValueError:
+            return set()
+        return {name for bit, name in cls.REASON_BITS if mask & bit}
+
     def summary(self):
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         rows = []
-        for line in open(self.path):
+        with open(self.path) as f:
+            lines = f.readlines()
+        os.unlink(self.path)
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
-                             "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7], "sw_power": parts[8]})
+                rows.append({"t": self._stamp(parts[0]), "sm": float(parts[2]), "max": float(parts[3]),
+                             "power": float(parts[4]), "active": parts[5], "hw": parts[6],
+                             "hw_thermal": parts[7], "sw_thermal": parts[8], "sw_power": parts[9]})
             except ValueError:
                 continue
-        os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        loaded = [r for r in rows if r["power"] > 300.0] or rows
-        reasons = set()
-        for r in loaded:
+        timed = all(r["t"] is not None for r in rows) and self.t0 is not None and self.t1 is not None
+        if timed:
+            window = [r for r in rows if self.t0 <= r["t"] <= self.t1]
+            if not window:
+                after = [r for r in rows if r["t"] >= self.t0]
+                window = after[:1] or rows[-1:]
+            selection = "timestamps inside the timed region"
+        else:
+            window = [r for r in rows if r["power"] > 300.0] or rows
+            selection = "samples above 300 W (no usable timestamps)"
+        reasons, other = set(), set()
+        for r in window:
             for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
                               ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
                 if r[key].lower().startswith("active"):
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["max"] for r in rows),
-                "reasons": sorted(reasons), "samples": len(loaded),
-                "power_w_median": statistics.median(r["power"] for r in loaded)}
+            for name in self._active_names(r["active"]):
+                (reasons if name in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+                 else other).add(name)
+        out = {"sm_mhz": statistics.median(r["sm"] for r in window), "sm_max_mhz": max(r["max"] for r in rows),
+               "reasons": sorted(reasons), "other_active": sorted(other - {"gpu_idle"}), "samples": len(window),
+               "sample_ms": self.PERIOD_MS, "selection": selection,
+               "power_w_median": statistics.median(r["power"] for r in window)}
+        if timed:
+            out["sm_mhz_min"] = min(r["sm"] for r in window)
+        return out
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -364,6 +422,7 @@ def run_ours(args, rank, world, local):
     with ClockSampler(local) as clocks:
         barrier()
         torch.cuda.synchronize()
+        clocks.mark_start()
         start.record(stream)
         marks[0].record(stream)
         for i in range(args.steps):
@@ -371,6 +430,7 @@ def run_ours(args, rank, world, local):
             marks[i + 1].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
+        clocks.mark_end()
         barrier()
     total_ms = start.elapsed_time(end)
     step_ms = sorted(marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps))

@@ -63,3 +63,40 @@ def test_phase_fractions_split_the_gemm_time():
 def test_host_cpu_names_architecture_and_model():
     info = bench.host_cpu()
     assert info["uname_m"] and isinstance(info["cpu_model"], str) and info["cpu_model"]
+
+
+def test_clock_summary_keeps_the_timed_region_and_decodes_reasons(tmp_path):
+    # Rows as nvidia-smi prints them for ClockSampler.FIELDS: idle samples before
+    # and after the timed region, three loaded ones inside it.
+    rows = [
+        "2026/12/03 09:00:00.000, 0, 1980, 2070, 180.10, 0x0000000000000001, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/03 09:00:01.050, 0, 1530, 2070, 950.20, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "2026/12/03 09:00:01.100, 0, 1545, 2070, 960.00, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "2026/12/03 09:00:01.150, 0, 1500, 2070, 955.00, 0x0000000000000006, Not Active, Not Active, Not Active, Active",
+        "2026/12/03 09:00:03.000, 0, 2070, 2070, 200.00, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+    ]
+    path = tmp_path / "clocks.csv"
+    path.write_text("\n".join(rows) + "\n")
+    c = bench.ClockSampler(0)
+    c.proc, c.path = object(), str(path)
+    c.t0 = bench.ClockSampler._stamp("2026/12/03 09:00:01.000")
+    c.t1 = bench.ClockSampler._stamp("2026/12/03 09:00:01.200")
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 1530.0 and s["sm_mhz_min"] == 1500.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"] and s["other_active"] == ["applications_clocks_setting"]
+    assert s["selection"].startswith("timestamps")
+
+    # A region shorter than the sampling period keeps the first sample after it started.
+    path.write_text("\n".join(rows) + "\n")
+    c.path = str(path)
+    c.t0 = bench.ClockSampler._stamp("2026/12/03 09:00:01.010")
+    c.t1 = bench.ClockSampler._stamp("2026/12/03 09:00:01.020")
+    s = c.summary()
+    assert s["samples"] == 1 and s["sm_mhz"] == 1530.0 and s["reasons"] == ["sw_power_cap"]
+
+    # A thermal reason set only in the bitmask is still reported.
+    path.write_text(rows[1].replace("0x0000000000000004", "0x0000000000000044") + "\n")
+    c.path = str(path)
+    c.t0, c.t1 = bench.ClockSampler._stamp("2026/12/03 09:00:01.000"), bench.ClockSampler._stamp("2026/12/03 09:00:02")
+    assert bench.ClockSampler(0).summary()["reasons"] == ["nvidia-smi unavailable"]
+    assert c.summary()["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
