@@ -689,6 +689,29 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, u
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MN-major operand map (rows of `inner` elements, `outer` rows): when the
+// row length is a multiple of 64, a 3-D view (64 elements, rows, inner / 64
+// atoms; strides row_bytes and 128 bytes) whose 64 x 64 x 2 box fills both
+// swizzle atoms of a 128-wide tile half in one copy; otherwise the 2-D map
+// with 64 x 64 boxes. Every address the 3-D view can form lies inside the
+// matrix, and rows past `outer` read as zeros as in the 2-D map. Returns the
+// layout code the kernels read (kMnBox3d or kMnBoxes2d), 0 on failure.
+static int32_t make_map_mn(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (!enc) return 0;
+  if (inner % 64 == 0) {
+    cuuint64_t dims[3] = {64, outer, inner / 64};
+    cuuint64_t strides[2] = {row_bytes, 128};
+    cuuint32_t box[3] = {64, 64, 2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      return kMnBox3d;
+  }
+  return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, row_bytes, 64, 64) ? kMnBoxes2d : 0;
+}
+
 struct DeviceInfo {
   int sms = 0;
   bool ready = false;
@@ -880,6 +903,7 @@ struct Maps {
   CUtensorMap h_k, w_k, w_k_half, h_mn, w_mn, dh, dw;
   CUtensorMap opt_part;   // the fused optimizer's Vc x D dW buffer (several row chunks only)
   CUtensorMap s_store[2], s_k[2], s_mn[2];   // one set per staging buffer
+  int32_t h_mn_form = 0, w_mn_form = 0, s_mn_form = 0;   // make_map_mn's layout codes
 };
 
 static GemmParams base_params(const flce_problem& p, WsHeader* hdr) {
@@ -1067,8 +1091,8 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     dw.m_tiles = (int)ceil_div(cols, kBM);
     dw.n_tiles = d_tiles;
     dw.k_blocks = (int)ceil_div(rows, kBK);
-    dw.a_mn = 1;
-    dw.b_mn = 1;
+    dw.a_mn = mp.s_mn_form;
+    dw.b_mn = mp.h_mn_form;
     dw.n_fast = 1;
     dw.b_k0 = (int32_t)r0;
     dw.mode = rc == 0 ? EPI_STORE : EPI_REDUCE;
@@ -1108,8 +1132,8 @@ static flce_status run_backward(const flce_problem& p, const Plan& pl, const Map
     dh.m_tiles = (int)ceil_div(rows, kBM);
     dh.n_tiles = d_tiles;
     dh.k_blocks = (int)ceil_div(cols, kBK);
-    dh.a_mn = 0;
-    dh.b_mn = 1;
+    dh.a_mn = kKMajor;
+    dh.b_mn = mp.w_mn_form;
     dh.n_fast = 1;
     dh.b_k0 = (int32_t)v0;
     dh.mode = vi == 0 ? EPI_STORE : EPI_REDUCE;
@@ -1167,14 +1191,16 @@ static bool build_maps(const flce_problem& p, const Plan& pl, const void* H, con
   if (!make_map(&mp->w_k, bf, W, D, V, D * 2, 64, kBN)) return false;
   if (!make_map(&mp->w_k_half, bf, W, D, V, D * 2, 64, kBN / 2)) return false;
   if (!backward) return true;
-  if (!make_map(&mp->h_mn, bf, H, D, N, D * 2, 64, 64)) return false;
-  if (!make_map(&mp->w_mn, bf, W, D, V, D * 2, 64, 64)) return false;
+  if (!(mp->h_mn_form = make_map_mn(&mp->h_mn, H, D, N, D * 2))) return false;
+  if (!(mp->w_mn_form = make_map_mn(&mp->w_mn, W, D, V, D * 2))) return false;
   for (int b = 0; b < 2; ++b) {
     void* stage = ws + pl.off_stage[b];
     const uint64_t vc = (uint64_t)pl.vcu, nc = (uint64_t)pl.nc;
     if (!make_map(&mp->s_store[b], bf, stage, vc, nc, vc * 2, 64, 32)) return false;
     if (!make_map(&mp->s_k[b], bf, stage, vc, nc, vc * 2, 64, kBM)) return false;
-    if (!make_map(&mp->s_mn[b], bf, stage, vc, nc, vc * 2, 64, 64)) return false;
+    const int32_t form = make_map_mn(&mp->s_mn[b], stage, vc, nc, vc * 2);
+    if (!form || (b == 1 && form != mp->s_mn_form)) return false;
+    mp->s_mn_form = form;
   }
   if (!make_map(&mp->dh, f32, dH, D, N, D * 4, 32, 32)) return false;
   if (dW && !make_map(&mp->dw, f32, dW, D, V, D * 4, 32, 32)) return false;
@@ -1271,7 +1297,7 @@ static flce_status run_backward_sorted(const flce_problem& p, const Plan& pl, co
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   if (!make_map(&ms.w_k, bf, w_sorted, D, V, D * 2, 64, kBN)) return FLCE_ERR_CUDA;
   if (!make_map(&ms.w_k_half, bf, w_sorted, D, V, D * 2, 64, kBN / 2)) return FLCE_ERR_CUDA;
-  if (!make_map(&ms.w_mn, bf, w_sorted, D, V, D * 2, 64, 64)) return FLCE_ERR_CUDA;
+  if (!(ms.w_mn_form = make_map_mn(&ms.w_mn, w_sorted, D, V, D * 2))) return FLCE_ERR_CUDA;
   // Ignored rows carry target -1 in the sorted problem: a valid sorted
   // position can equal the caller's ignore index when that lies in [0, V).
   flce_problem ps = p;

@@ -80,13 +80,23 @@ constexpr uint32_t kDevBadTarget = 1u;
 constexpr uint32_t kDevTimeout = 2u;
 constexpr uint32_t kDevBadHparams = 4u;
 
+// How an operand's k-block reaches shared memory. K-major: one box of 64 k
+// (128 bytes) by the tile's rows. MN-major (k varies slowest in global
+// memory): each 64-element-wide, 128-byte-swizzled atom of the tile is one
+// 2-D box of 64 x 64 (kMnBoxes2d), or the map views the rows as (64
+// elements, k, atoms) and one 3-D box brings two neighbouring atoms
+// (kMnBox3d). The 3-D view needs the row length to be a multiple of 64;
+// measured at the Gravity head shape it took the dW and dH k-blocks from
+// 560-565 to 530-537 cycles, with bit-identical results.
+constexpr int32_t kKMajor = 0, kMnBoxes2d = 1, kMnBox3d = 2;
+
 // Each problem's parameters start on a 128-byte boundary of the launch's
 // parameter block. Measured on GB300 with the same sources otherwise: with
 // sizes of 224, 264 or 320 bytes (or 64-byte alignment) the forward launch ran
 // about 11% slower, at higher SM clocks, than with 128-byte alignment.
 struct alignas(128) GemmParams {
   int32_t m_tiles, n_tiles, k_blocks;
-  int32_t a_mn, b_mn;          // 1 if the operand is MN-major in global memory
+  int32_t a_mn, b_mn;          // operand layout: kKMajor, kMnBoxes2d or kMnBox3d
   int32_t n_fast;              // tile raster: 1 = n index varies fastest
   int32_t a_m0, a_k0;          // coordinate offsets of A (M and K directions)
   int32_t b_n0, b_k0;          // coordinate offsets of B (N and K directions)
@@ -672,13 +682,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_kernel(const __grid
           uint8_t* sb = sa + kABytes;
           ptx::mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
           const int32_t kc = kb * kBK;
-          if (p.a_mn) {
+          if (p.a_mn == kMnBox3d) {
+            ptx::tma_load_3d(sa, tmA, 0, p.a_k0 + kc, (p.a_m0 + mt * kBM) >> 6, &full_bar[stage]);
+          } else if (p.a_mn) {
             for (int h = 0; h < kBM / 64; ++h)
               ptx::tma_load_2d(sa + h * 8192, tmA, p.a_m0 + mt * kBM + h * 64, p.a_k0 + kc, &full_bar[stage]);
           } else {
             ptx::tma_load_2d(sa, tmA, p.a_k0 + kc, p.a_m0 + mt * kBM, &full_bar[stage]);
           }
-          if (p.b_mn) {
+          if (p.b_mn == kMnBox3d) {
+            for (int h = 0; h < kBN / 128; ++h)
+              ptx::tma_load_3d(sb + h * 16384, tmB, 0, p.b_k0 + kc, ((p.b_n0 + nt * kBN) >> 6) + 2 * h,
+                               &full_bar[stage]);
+          } else if (p.b_mn) {
             for (int h = 0; h < kBN / 64; ++h)
               ptx::tma_load_2d(sb + h * 8192, tmB, p.b_n0 + nt * kBN + h * 64, p.b_k0 + kc, &full_bar[stage]);
           } else {

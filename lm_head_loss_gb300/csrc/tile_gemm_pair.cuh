@@ -170,13 +170,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) flce_gemm_pair_kernel(const _
           const uint32_t fb = full_leader + stage * 8u;
           if (leader) ptx::mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
           const int32_t kc = kb * kBK;
-          if (a_mn) {
+          if (a_mn == kMnBox3d) {
+            ptx::tma_load_3d_pair(sa, tmA, 0, a_k + kc, a_m >> 6, fb);
+          } else if (a_mn) {
             ptx::tma_load_2d_pair(sa, tmA, a_m, a_k + kc, fb);
             ptx::tma_load_2d_pair(sa + 8192, tmA, a_m + 64, a_k + kc, fb);
           } else {
             ptx::tma_load_2d_pair(sa, tmA, a_k + kc, a_m, fb);
           }
-          if (b_mn) {
+          if (b_mn == kMnBox3d) {
+            ptx::tma_load_3d_pair(sb, tmB, 0, b_k + kc, b_n >> 6, fb);
+          } else if (b_mn) {
             ptx::tma_load_2d_pair(sb, tmB, b_n, b_k + kc, fb);
             ptx::tma_load_2d_pair(sb + 8192, tmB, b_n + 64, b_k + kc, fb);
           } else {
