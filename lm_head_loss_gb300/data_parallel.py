@@ -28,6 +28,7 @@ from typing import Callable
 import torch
 
 from . import _binding as B
+from .api import _check_inputs
 
 
 def exchange_step(local_count: Callable[[], torch.Tensor],
@@ -88,9 +89,12 @@ class DataParallelStep:
         """Runs on torch's current stream, the stream torch.distributed's
         NCCL all-reduces order themselves with."""
         p = self.problem
-        stream = torch.cuda.current_stream(self.device)
+        _check_inputs(H, W, y)
         if H.shape != (p.n_rows, p.hidden) or W.shape != (p.vocab, p.hidden) or y.shape != (p.n_rows,):
             raise ValueError("H, W, y do not match the shapes this step was built for")
+        if not (H.device == W.device == y.device == self.ws.device):
+            raise ValueError(f"H, W and y must be on {self.ws.device}, the device of this step's buffers")
+        stream = torch.cuda.current_stream(self.device)
 
         def local_count():
             st = B.flce_count_valid(p, y, self.count, stream)

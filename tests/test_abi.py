@@ -213,6 +213,21 @@ def test_api_refuses_cpu_tensors():
         flce.forward(H, W, y)
 
 
+def test_data_parallel_step_refuses_cpu_tensors():
+    # The step's buffers need a GPU; the check on the inputs comes first, so a
+    # step object without them is enough to see CPU tensors refused.
+    import torch
+    step = object.__new__(flce.DataParallelStep)
+    step.problem = flce.make_problem(4, 8, 5)
+    H = torch.zeros(4, 8, dtype=torch.bfloat16)
+    W = torch.zeros(5, 8, dtype=torch.bfloat16)
+    y = torch.zeros(4, dtype=torch.int64)
+    with pytest.raises(ValueError, match="CUDA"):
+        step(H, W, y)
+    with pytest.raises(TypeError):
+        step(H.float(), W, y)
+
+
 def test_data_parallel_calls_reject_bad_arguments_on_the_host():
     # Rejected before any launch, so this runs without a GPU.
     p = flce.make_problem(64, 128, 1000)
