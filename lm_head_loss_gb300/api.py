@@ -27,6 +27,20 @@ def _check_inputs(H: torch.Tensor, W: torch.Tensor, y: torch.Tensor):
         raise ValueError("H, W and y must be contiguous")
 
 
+def _check_out(out, H: torch.Tensor, W: torch.Tensor):
+    """`out` = (loss, lse, dH, dW) written by the kernels: fp32, contiguous, on
+    H's device, with the shapes the call writes (the library sees only
+    pointers, so a smaller buffer would be written past its end)."""
+    if len(out) != 4:
+        raise ValueError("out must be (loss, lse, dH, dW)")
+    n, d, v = H.shape[0], H.shape[1], W.shape[0]
+    for t, shape, name in zip(out, ((), (n,), (n, d), (v, d)), ("loss", "lse", "dH", "dW")):
+        ok_shape = t.numel() == 1 if name == "loss" else tuple(t.shape) == shape
+        if (not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not ok_shape or t.device != H.device
+                or not t.is_contiguous()):
+            raise ValueError(f"out {name} must be a contiguous fp32 tensor of shape {shape} on {H.device}")
+
+
 class Workspace:
     """A reusable device workspace (a torch uint8 buffer) grown on demand."""
 
@@ -72,6 +86,7 @@ def forward_backward(H, W, y, grad_loss: float = 1.0, ignore_index: int = -100, 
         dH = torch.empty(H.shape, dtype=torch.float32, device=H.device)
         dW = torch.empty(W.shape, dtype=torch.float32, device=H.device)
     else:
+        _check_out(out, H, W)
         loss, lse, dH, dW = out
     st = B.flce_forward_backward(prob, H, W, y, grad_loss, lse, loss, dH, dW, ws, stream=stream)
     if st != B.Status.OK:

@@ -242,3 +242,23 @@ def test_data_parallel_calls_reject_bad_arguments_on_the_host():
                 stream=0) == Status.ERR_INVALID_ARGUMENT
     assert call(p, FAKE, FAKE, FAKE, FAKE, 1.0, None, FAKE, FAKE, FAKE, FAKE, ws_bytes=nb - 1,
                 stream=0) == Status.ERR_WORKSPACE_TOO_SMALL
+
+
+def test_caller_output_buffers_are_checked_before_use():
+    # forward_backward(out=...) hands these pointers to kernels that write the
+    # full shapes; a short or mistyped buffer must be refused on the host.
+    import torch
+    from lm_head_loss_gb300.api import _check_out
+    H = torch.zeros(4, 8, dtype=torch.bfloat16)
+    W = torch.zeros(5, 8, dtype=torch.bfloat16)
+    good = (torch.zeros(()), torch.zeros(4), torch.zeros(4, 8), torch.zeros(5, 8))
+    _check_out(good, H, W)
+    bad = [(torch.zeros(()), torch.zeros(4), torch.zeros(4, 8), torch.zeros(4, 8)),       # dW too short
+           (torch.zeros(()), torch.zeros(3), torch.zeros(4, 8), torch.zeros(5, 8)),       # lse too short
+           (torch.zeros(()), torch.zeros(4), torch.zeros(4, 8).double(), torch.zeros(5, 8)),
+           (torch.zeros(()), torch.zeros(4), torch.zeros(8, 4).t(), torch.zeros(5, 8)),   # not contiguous
+           (torch.zeros(2), torch.zeros(4), torch.zeros(4, 8), torch.zeros(5, 8)),
+           good[:3]]
+    for out in bad:
+        with pytest.raises(ValueError):
+            _check_out(out, H, W)
